@@ -1,0 +1,162 @@
+"""Seeded synthetic inputs for the sparse decode step.
+
+This module only draws random numbers and fixes shapes. It computes nothing of
+the method itself (no paging arithmetic, no scores, no selection, no
+attention), so that both the CUDA path and the CPU oracle can take their inputs
+from it without sharing any of the method's arithmetic.
+
+The five named workloads follow the shapes of the long-context,
+high-concurrency decode workloads that the sources describe ("Sparse Attention
+on GLM5.3 and HBM", HiSparse section; "Paged KV cache", worked example):
+
+* ``paging_example``  - the five requests of the paged-KV worked example
+  (403/96/241/30/176 tokens, 16-token pages), small enough for the oracle.
+* ``b32_4k``          - 32 x 4096 tokens, 64-token pages, pool pages permuted.
+* ``b64_ragged_prefix`` - 64 ragged requests (1k-32k tokens), groups of 8
+  sharing a 2000-token prefix, 16-token pages.
+* ``b16_128k``        - 16 x 131072 tokens, 4-head indexer, top-2048.
+* ``b256_8k_lru``     - 256 x 8192 tokens, HBM slot table holding half of the
+  pages (LRU), compacted miss list per step.
+
+Value distributions: K/V and attention queries are N(0, 1) rounded to bf16
+(round to nearest even); indexer queries and keys are integers uniform in
+[-127, 127]; indexer head weights are all one ("summed").
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    """Shape of one decode-step workload.
+
+    ``seq_lens`` fixes the request lengths outright; otherwise they are drawn
+    uniformly from ``[len_lo, len_hi]``.  ``group_size > 0`` puts consecutive
+    blocks of ``group_size`` requests into prefix groups sharing the first
+    ``prefix_len`` tokens.  ``num_pages`` is the size of the physical page pool
+    (an upper bound on what the requests need), ``max_pages`` the width of a
+    block-table row.  ``capacity > 0`` enables the HBM residency table with that
+    many slots, initially holding ``initial_resident`` randomly chosen pages.
+    """
+
+    name: str
+    B: int
+    page_size: int
+    Hq: int
+    Hkv: int
+    D: int
+    Hi: int
+    Di: int
+    k: int
+    num_pages: int
+    max_pages: int
+    seed: int
+    seq_lens: Optional[tuple] = None
+    len_lo: int = 0
+    len_hi: int = 0
+    prefix_len: int = 0
+    group_size: int = 0
+    permute_pool: bool = False
+    capacity: int = 0
+    initial_resident: int = 0
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def max_len(self) -> int:
+        return self.max_pages * self.page_size
+
+
+WORKLOADS = {
+    "paging_example": Workload(
+        name="paging_example", B=5, seq_lens=(403, 96, 241, 30, 176), page_size=16,
+        Hq=8, Hkv=2, D=64, Hi=1, Di=64, k=64, num_pages=64, max_pages=32, seed=0),
+    "b32_4k": Workload(
+        name="b32_4k", B=32, seq_lens=(4096,) * 32, page_size=64, Hq=32, Hkv=8, D=128,
+        Hi=1, Di=128, k=512, num_pages=2048, max_pages=64, seed=1, permute_pool=True),
+    "b64_ragged_prefix": Workload(
+        name="b64_ragged_prefix", B=64, len_lo=1024, len_hi=32768, page_size=16,
+        Hq=32, Hkv=8, D=128, Hi=1, Di=128, k=2048, num_pages=64 * 2048, max_pages=2048,
+        seed=2, prefix_len=2000, group_size=8),
+    "b16_128k": Workload(
+        name="b16_128k", B=16, seq_lens=(131072,) * 16, page_size=64, Hq=64, Hkv=8,
+        D=128, Hi=4, Di=128, k=2048, num_pages=16 * 2048, max_pages=2048, seed=3),
+    "b256_8k_lru": Workload(
+        name="b256_8k_lru", B=256, seq_lens=(8192,) * 256, page_size=64, Hq=32, Hkv=8,
+        D=128, Hi=1, Di=128, k=1024, num_pages=256 * 128, max_pages=128, seed=4,
+        capacity=16384, initial_resident=16384),
+}
+
+#: the workloads in the order they are listed above
+WORKLOAD_ORDER = ["paging_example", "b32_4k", "b64_ragged_prefix", "b16_128k", "b256_8k_lru"]
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def draw_host(wl: Workload) -> dict:
+    """Small host-side draws (CPU generator, independent of where tensors live).
+
+    Returns int32 CPU tensors: ``seq_lens`` [B]; ``prefix_group`` [B] (-1 = no
+    group) or None; ``free_order`` [num_pages] (a permutation of the pool) or
+    None for the ascending pool; ``initial_resident`` (sorted page ids) or None.
+    """
+    g = _gen("cpu", wl.seed)
+    if wl.seq_lens is not None:
+        assert len(wl.seq_lens) == wl.B
+        seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32)
+    else:
+        seq_lens = torch.randint(wl.len_lo, wl.len_hi + 1, (wl.B,), generator=g,
+                                 dtype=torch.int64).to(torch.int32)
+    prefix_group = None
+    if wl.group_size > 0:
+        prefix_group = (torch.arange(wl.B, dtype=torch.int32) // wl.group_size).to(torch.int32)
+    free_order = None
+    if wl.permute_pool:
+        free_order = torch.randperm(wl.num_pages, generator=g, dtype=torch.int64).to(torch.int32)
+    initial_resident = None
+    if wl.capacity > 0:
+        pick = torch.randperm(wl.num_pages, generator=g, dtype=torch.int64)[: wl.initial_resident]
+        initial_resident = torch.sort(pick).values.to(torch.int32)
+    return dict(seq_lens=seq_lens, prefix_group=prefix_group, free_order=free_order,
+                initial_resident=initial_resident)
+
+
+def draw_tensors(wl: Workload, device="cpu", seed_offset: int = 0) -> dict:
+    """Large draws on ``device``: query tensors and the physical page pools.
+
+    ``seed_offset`` gives a fresh query set over the same shapes (used to vary
+    the selection between steps).  Returns: ``q`` bf16 [B, Hq, D]; ``q_idx``
+    int8 [B, Hi, Di]; ``w_idx`` int32 [Hi] (ones); ``kv_k`` / ``kv_v`` bf16
+    [num_pages, page_size, Hkv, D]; ``idx_k`` int8 [num_pages, page_size, Di].
+    """
+    g = _gen(device, wl.seed * 1000003 + 7919 * seed_offset + 17)
+    P = wl.page_size
+    pool = (wl.num_pages, P, wl.Hkv, wl.D)
+    kv_k = torch.randn(pool, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    kv_v = torch.randn(pool, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    idx_k = torch.randint(-127, 128, (wl.num_pages, P, wl.Di), generator=g, device=device,
+                          dtype=torch.int8)
+    q, q_idx = draw_queries(wl, device, seed_offset)
+    w_idx = torch.ones(wl.Hi, dtype=torch.int32, device=device)
+    return dict(q=q, q_idx=q_idx, w_idx=w_idx, kv_k=kv_k, kv_v=kv_v, idx_k=idx_k)
+
+
+def draw_queries(wl: Workload, device="cpu", seed_offset: int = 0):
+    """Per-step query draws: ``q`` bf16 [B, Hq, D] and ``q_idx`` int8 [B, Hi, Di]."""
+    g = _gen(device, wl.seed * 7777 + 104729 * (seed_offset + 1) + 3)
+    q = torch.randn((wl.B, wl.Hq, wl.D), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    q_idx = torch.randint(-127, 128, (wl.B, wl.Hi, wl.Di), generator=g, device=device,
+                          dtype=torch.int8)
+    return q, q_idx
