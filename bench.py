@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse decode step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pks|reference]
+
+One step = the whole hot path over one batch: int8 indexer scan of every
+cached token, exact top-k, paged sparse attention (plus the residency update
+for the workload with an HBM slot table).  Default workload: 16 requests x
+131072 tokens, 64-token pages, GQA 64/8, head dim 128, 4-head int8 indexer,
+top-2048.  Inputs are seeded synthetic tensors resident in HBM; L2 is flushed
+(256 MB write) between timed steps, outside the timed intervals.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica batch (weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from top_sparse_attention_pks_gb300 import build as pkg_build  # noqa: E402
+from top_sparse_attention_pks_gb300 import pks  # noqa: E402
+from top_sparse_attention_pks_gb300.decoder import SparseDecodeStep  # noqa: E402
+from top_sparse_attention_pks_gb300.workloads import (WORKLOADS, draw_host,  # noqa: E402
+                                                      draw_tensors)
+
+METRIC = "sparse decode steps/s"
+UNIT = "steps/s"
+NOMINAL_HBM_GBS = 8000.0  # the roofline denominator the target is stated against
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ setup --
+
+def setup(wl, device, seed_offset=0):
+    h = draw_host(wl)
+    pool = pks.Pool(wl.num_pages, wl.page_size, h["free_order"])
+    bt, _ = pool.build_block_table(h["seq_lens"], wl.max_pages, h["prefix_group"], wl.prefix_len)
+    pool.close()
+    t = draw_tensors(wl, device, seed_offset)
+    t["seq_lens"] = h["seq_lens"].to(device)
+    t["block_table"] = torch.from_numpy(bt).to(device)
+    return t, h, bt
+
+
+def algorithmic_bytes(wl, lens, bt, topk):
+    """Unique physical bytes of one step: indexer keys scanned, K/V rows
+    gathered, outputs written (aliased prefix pages counted once)."""
+    P = wl.page_size
+    scan_rows, kv_rows = [], []
+    for b, n in enumerate(lens):
+        n = int(n)
+        if n == 0:
+            continue
+        t = np.arange(n, dtype=np.int64)
+        scan_rows.append(bt[b, t // P].astype(np.int64) * P + t % P)
+        sel = topk[b][topk[b] >= 0].astype(np.int64)
+        kv_rows.append(bt[b, sel // P].astype(np.int64) * P + sel % P)
+    n_scan = np.unique(np.concatenate(scan_rows)).size if scan_rows else 0
+    n_kv = np.unique(np.concatenate(kv_rows)).size if kv_rows else 0
+    scan = n_scan * wl.Di
+    kv = n_kv * wl.Hkv * wl.D * 2 * 2
+    out = wl.B * wl.Hq * wl.D * 2
+    attended = int(sum(min(int(n), wl.k) for n in lens))
+    return dict(scan=scan, kv=kv, out=out, total=scan + kv + out, attended=attended)
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = Path(os.environ.get("TMPDIR", "/tmp")) / f"pks_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in self.path.read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                 reasons=parts[5:9]))
+            except ValueError:
+                continue
+        self.path.unlink(missing_ok=True)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        active = sorted({names[i] for r in rows for i, v in enumerate(r["reasons"])
+                         if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["sm_max"] for r in rows),
+                "reasons": active, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ oracle arm --
+
+def oracle_request_step(wl, t_host, b, n_tokens):
+    """The oracle's whole step for request b truncated to n_tokens tokens."""
+    import oracle
+    P = wl.page_size
+    lens = np.array([n_tokens], np.int32)
+    scores = oracle.indexer_scores(lens, t_host["bt"][b: b + 1], P, t_host["q_idx"][b: b + 1],
+                                   t_host["w_idx"], t_host["idx_k"])
+    idx = oracle.topk(lens, scores, wl.k)
+    oracle.sparse_attention(t_host["bt"][b: b + 1], P, idx, t_host["q"][b: b + 1],
+                            t_host["kv_k"], t_host["kv_v"])
+
+
+def oracle_inputs(wl, t, b):
+    """Host copies of request b's pages, remapped to a compact pool."""
+    lens = t["seq_lens"].cpu().numpy()
+    bt = t["block_table"].cpu().numpy()
+    n_pages = -(-int(lens[b]) // wl.page_size)
+    pages = torch.from_numpy(bt[b, :n_pages].astype(np.int64)).to(t["kv_k"].device)
+    cbt = np.full((wl.B, wl.max_pages), -1, np.int32)
+    cbt[b, :n_pages] = np.arange(n_pages)
+    return dict(bt=cbt, q_idx=t["q_idx"].cpu().numpy(), w_idx=t["w_idx"].cpu().numpy(),
+                q=t["q"].cpu(), idx_k=t["idx_k"].index_select(0, pages).cpu().numpy(),
+                kv_k=t["kv_k"].index_select(0, pages).cpu(),
+                kv_v=t["kv_v"].index_select(0, pages).cpu(), len=int(lens[b]))
+
+
+def time_oracle(wl, t, budget_s, min_reps=1, steps=None, warmup=0):
+    """Time the oracle on request 0 (longest-context request of the batch)."""
+    import oracle
+    cores = oracle.set_threads(0)
+    lens = t["seq_lens"].cpu().numpy()
+    b = int(np.argmax(lens))
+    hi = oracle_inputs(wl, t, b)
+    full = hi["len"]
+    # calibrate on a slice, then choose the slice each timed step covers
+    n0 = min(full, max(4 * wl.k, 8192))
+    t0 = time.perf_counter()
+    oracle_request_step(wl, hi, b, n0)
+    c = (time.perf_counter() - t0) / n0
+    n_steps = steps if steps is not None else None
+    if n_steps is None:
+        n_tok = full
+    else:
+        per_step = budget_s / max(1, n_steps + warmup)
+        n_tok = int(min(full, max(min(full, 4 * wl.k), per_step / max(c, 1e-12))))
+    for _ in range(warmup):
+        oracle_request_step(wl, hi, b, n_tok)
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        s = time.perf_counter()
+        oracle_request_step(wl, hi, b, n_tok)
+        times.append(time.perf_counter() - s)
+        if n_steps is not None:
+            if len(times) >= n_steps:
+                break
+        elif len(times) >= min_reps and time.perf_counter() - t_start >= budget_s:
+            break
+    mean = sum(times) / len(times)
+    total_tokens = float(lens.sum())
+    step_time = mean * total_tokens / n_tok  # scaled to the whole batch
+    sample = (f"request {b} ({full} tokens) truncated to {n_tok} tokens per timed step, "
+              f"{len(times)} steps; time scaled by tokens to the {wl.B}-request batch "
+              f"({int(total_tokens)} tokens)")
+    return dict(value=1.0 / step_time, unit=UNIT, cores=cores, kind="oracle", sample=sample,
+                step_seconds=step_time, reps=len(times))
+
+
+# ------------------------------------------------------------------ main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="b16_128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="pks", choices=["pks", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage-steps", type=int, default=200)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "pks" else "gloo")
+    if args.impl == "reference" and rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        pkg_build.build_library()
+    if dist:
+        dist.barrier()
+    wl = WORKLOADS[args.workload]
+    t, h, bt = setup(wl, dev, seed_offset=rank)
+
+    if args.impl == "reference":
+        ref = time_oracle(wl, t, budget_s=120.0, steps=args.steps, warmup=args.warmup)
+        line = {"impl": "reference", "metric": METRIC, "value": ref["value"], "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ref["step_seconds"] * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
+                "data": "synthetic", "config": config_dict(wl, args),
+                "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores", "kind",
+                                                     "sample")},
+                "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    step = SparseDecodeStep(t, wl.k)
+    res = None
+    miss = n_miss = None
+    if wl.capacity > 0:
+        res = pks.ResidencyTable(wl.num_pages, wl.capacity, h["initial_resident"].numpy(),
+                                 device=dev)
+        miss = torch.empty(wl.num_pages, dtype=torch.int32, device=dev)
+        n_miss = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+
+    def one_step(stream):
+        step(stream)
+        if res is not None:
+            res.update(step.topk_idx, t["block_table"], wl.page_size, miss, n_miss, stream)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            one_step(s)
+    torch.cuda.synchronize()
+    if step.device_error(s) != 0:
+        raise RuntimeError("device-side check fired during warm-up")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        one_step(s)
+    launches_per_step = 4 + (2 if res is not None else 0)
+
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush.zero_()
+            g.replay()
+    torch.cuda.synchronize()
+    topk_host = step.topk_idx.cpu().numpy()
+    ab = algorithmic_bytes(wl, h["seq_lens"].numpy(), bt, topk_host)
+
+    # ---- timed region: K graph replays, each bracketed by events; L2 flushed
+    # between steps outside the intervals
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the work
+    with torch.cuda.stream(s):
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(s)
+            g.replay()
+            ends[i].record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_s = sum(step_ms) / 1e3
+    if dist:
+        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+    value = world * args.steps / total_s
+    ms_per_step = total_s * 1e3 / args.steps
+
+    # ---- per-stage times inside the real step (events between the stages)
+    stage = {"scan": [], "topk": [], "attention": []}
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for _ in range(args.stage_steps)]
+    with torch.cuda.stream(s):
+        for row in evs:  # torch creates the CUDA events on first record
+            for e in row:
+                e.record(s)
+        for i in range(args.stage_steps):
+            flush.zero_()
+            step.timed(evs[i], s)
+    torch.cuda.synchronize()
+    for e in evs:
+        stage["scan"].append(e[0].elapsed_time(e[1]))
+        stage["topk"].append(e[1].elapsed_time(e[2]))
+        stage["attention"].append(e[2].elapsed_time(e[3]))
+    stage_ms = {k: sum(v) / len(v) for k, v in stage.items()}
+    peak, peak_kind = measured_peaks()
+    kern_bytes = {"scan": ab["scan"], "attention": ab["kv"] + ab["out"]}
+    dominant = max(("scan", "attention"), key=lambda k: stage_ms[k])
+    achieved = kern_bytes[dominant] / (stage_ms[dominant] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": {"scan": "k_indexer_scan",
+                                           "attention": "k_sparse_attention"}[dominant],
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy test)",
+                "traffic": profiled_traffic(dominant, wl.name),
+                "algorithmic_bytes_per_launch": kern_bytes[dominant],
+                "launch_ms": stage_ms[dominant]}
+    step_gbs = ab["total"] / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the public call with host buffers
+    e2e = end_to_end(step, t, wl, args, s, flush, res, miss, n_miss)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = time_oracle(wl, t, budget_s=15.0)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": config_dict(wl, args),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+            "step_hbm": {"algorithmic_bytes": ab["total"], "scan_bytes": ab["scan"],
+                         "kv_bytes": ab["kv"], "out_bytes": ab["out"],
+                         "achieved_gbs": step_gbs,
+                         "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                         "frac_of_measured": step_gbs / peak},
+            "tokens_attended_per_s": ab["attended"] * value,
+            "stages_ms": stage_ms,
+            "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def config_dict(wl, args):
+    return {"workload": wl.name, "requests": wl.B,
+            "seq_len": list(wl.seq_lens) if wl.seq_lens and len(set(wl.seq_lens)) > 1
+            else (wl.seq_lens[0] if wl.seq_lens else f"U[{wl.len_lo},{wl.len_hi}]"),
+            "page_size": wl.page_size, "heads_q_kv": [wl.Hq, wl.Hkv], "head_dim": wl.D,
+            "indexer_heads_dim": [wl.Hi, wl.Di], "indexer_dtype": "int8", "top_k": wl.k,
+            "kv_dtype": "bf16", "prefix": [wl.prefix_len, wl.group_size],
+            "residency_slots": wl.capacity, "parallelism": f"replicas x{args.gpus}",
+            "l2": "flushed between timed steps (256 MB write, outside the timed intervals)",
+            "timing": "CUDA events around each CUDA-graph replay of the step"}
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    import hashlib
+    src = ROOT / "top_sparse_attention_pks_gb300" / "csrc" / (
+        "k_indexer.cu" if kernel == "scan" else "k_attention.cu")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    prof = ROOT / "profiles" / f"{'k_indexer_scan' if kernel == 'scan' else 'k_sparse_attention'}_{workload}.md"
+    if not prof.exists():
+        return None
+    kv = {}
+    for line in prof.read_text().splitlines():
+        if line.startswith("- ") and ":" in line:
+            key, _, val = line[2:].partition(":")
+            kv[key.strip()] = val.strip().strip("`")
+    if kv.get("source_sha256_16") != sha:
+        return None
+    try:
+        return int(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def end_to_end(step, t, wl, args, s, flush, res, miss, n_miss):
+    """Per step: pinned host -> device copy of the step's inputs (queries,
+    lengths, block table), the public pks_decode_step call, device -> pinned
+    host copy of the outputs (attention output, top-k), host synchronise."""
+    names = ["q", "q_idx", "seq_lens", "block_table"]
+    host_in = {n: t[n].cpu().pin_memory() for n in names}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    idx_h = torch.empty(step.topk_idx.shape, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = out_h.numel() * out_h.element_size() + idx_h.numel() * idx_h.element_size()
+    extra = []
+    if res is not None:
+        extra = [torch.empty(1, dtype=torch.int32).pin_memory()]
+        d2h += 4
+    n = min(args.steps, 500)
+    total = 0.0
+    with torch.cuda.stream(s):
+        for i in range(n + 3):
+            flush.zero_()
+            s.synchronize()
+            t0 = time.perf_counter()
+            for nm in names:
+                t[nm].copy_(host_in[nm], non_blocking=True)
+            pks.pks_decode_step(step.args, s)
+            if res is not None:
+                res.update(step.topk_idx, t["block_table"], wl.page_size, miss, n_miss, s)
+                extra[0].copy_(n_miss, non_blocking=True)
+            out_h.copy_(step.out, non_blocking=True)
+            idx_h.copy_(step.topk_idx, non_blocking=True)
+            s.synchronize()
+            if i >= 3:
+                total += time.perf_counter() - t0
+    return {"value": n / total, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n,
+            "timing": "host wall clock per step incl. copies and stream synchronise"}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,227 @@
+/*
+ * pks - top-k sparse attention decode over a paged KV cache, for GB300 (sm_103a).
+ *
+ * C ABI of libpks.so.  Plain integers, sizes and pointers only; every
+ * function returns a pks_status and never aborts.  Device work is enqueued
+ * on the caller's stream and does not synchronise; the library allocates no
+ * device memory (scratch comes from a caller-owned workspace) and keeps no
+ * global state.
+ *
+ * Sources, cited by title and section:
+ *  [SA]  "Sparse Attention on GLM5.3 and HBM": introduction (top-k tokens,
+ *        SDPA over only those; the selection needs the whole context in HBM),
+ *        HiSparse paragraph (LRU cache of KV in HBM, load on a top-k miss,
+ *        evict by least recent use), DeepSeek Sparse Attention paragraph
+ *        (lightning indexer: multi-head query, single-head key, dot product,
+ *        ReLU, weighted sum over heads; one top-K set shared by all heads;
+ *        dense attention below K tokens).
+ *  [PKV] "Paged KV cache, or why reserving for the maximum length is
+ *        wasteful": "Paging" (fixed-size pages, a per-request page table,
+ *        pages = ceil(len / page_size)), "Page sharing" (identical prefixes
+ *        point to the same pages, only whole pages are shared), "What this
+ *        table does not say" (free-page list, page tables, scattered reads).
+ *  [LIN] "Why recalling an old conversation costs so much", "Three blockers":
+ *        a store that takes logical slot ids must translate them to physical
+ *        ids (here: token positions are always logical, only the block table
+ *        maps them to pages); a pool sized outside the memory accounting
+ *        crashed at start-up (here: no hidden allocation).
+ *
+ * Layouts (all row-major, all device pointers unless stated "host"):
+ *   q            bf16  [B, Hq, D]            attention query of the decoded token
+ *   q_idx        int8  [B, Hi, Di]           indexer query (Hi heads)
+ *   w_idx        int32 [Hi]                  indexer head weights
+ *   kv_k, kv_v   bf16  [num_pages, page_size, Hkv, D]   paged K / V pools
+ *   idx_k        int8  [num_pages, page_size, Di]       paged single-head indexer keys
+ *   seq_lens     int32 [B]                   cached tokens per request (0 allowed)
+ *   block_table  int32 [B, max_pages]        logical page -> physical page; entries at
+ *                                            p >= ceil(len_b/page_size) are ignored
+ *   topk_idx     int32 [B, k]                selected logical token positions, ascending,
+ *                                            padded with -1
+ *   out          bf16  [B, Hq, D]            attention output
+ * Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
+ */
+#ifndef PKS_H
+#define PKS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t / cudaEvent_t, passed without the CUDA headers. NULL = legacy default stream. */
+typedef struct CUstream_st* pks_stream;
+typedef struct CUevent_st* pks_event;
+
+typedef int32_t pks_status;
+#define PKS_OK 0
+#define PKS_ERR_INVALID (-1)      /* bad argument: null pointer, negative or inconsistent size */
+#define PKS_ERR_OOM (-2)          /* host page pool cannot satisfy the request (nothing taken) */
+#define PKS_ERR_CUDA (-3)         /* a CUDA runtime call (launch, copy, memset) failed */
+#define PKS_ERR_TIMEOUT (-4)      /* a bounded device-side wait ran out */
+#define PKS_ERR_DEVICE_CHECK (-5) /* a device-side bounds check fired (see *_device_error) */
+#define PKS_ERR_UNSUPPORTED (-6)  /* valid but outside the compiled shapes (see pks_decode_args) */
+#define PKS_ERR_WORKSPACE (-7)    /* workspace missing, misaligned or smaller than required */
+
+/* Static English text for a status code. */
+const char* pks_status_str(pks_status status);
+
+/* ------------------------------------------------------------------------
+ * Host page allocator ([PKV] "Paging", "What this table does not say").
+ * A pool of num_pages physical pages of page_size tokens with a FIFO free
+ * list: pages are handed out from the front, freed pages go to the back.
+ * The initial order is 0..num_pages-1, or the permutation free_order (host,
+ * num_pages entries, copied).  The handle is host memory owned by the
+ * library; it is not thread-safe.
+ * ---------------------------------------------------------------------- */
+typedef struct pks_pool pks_pool;
+
+/* INVALID: num_pages < 1, page_size < 1, free_order not a permutation, out NULL. */
+pks_status pks_pool_create(int32_t num_pages, int32_t page_size, const int32_t* free_order,
+                           pks_pool** out);
+void pks_pool_destroy(pks_pool* pool);
+pks_status pks_pool_free_count(const pks_pool* pool, int32_t* out);
+
+/* Take n pages from the front of the free list into out_ids (host, n entries).
+ * All or nothing: OOM (and nothing taken) when fewer than n are free. */
+pks_status pks_alloc_pages(pks_pool* pool, int32_t n, int32_t* out_ids);
+
+/* Return n pages (host ids) to the back of the free list.  INVALID (and
+ * nothing returned) if an id is out of range, already free, or repeated. */
+pks_status pks_free_pages(pks_pool* pool, int32_t n, const int32_t* ids);
+
+/* [PKV] "Paging" + "Page sharing": build the block table of a batch.
+ * Requests are served in ascending order; request b takes ceil(len_b /
+ * page_size) logical pages, in ascending order, each from pks_alloc_pages.
+ * Prefix sharing: when prefix_group (host, nullable) gives request b a group
+ * id >= 0, its logical page p is an alias of the page an earlier member of
+ * the same group holds at p, provided the page lies wholly inside the shared
+ * prefix and wholly inside request b (p < floor(prefix_len / page_size) and
+ * p < floor(len_b / page_size)); otherwise a fresh page is taken.  So a group
+ * of n requests at least prefix_len long saves (n-1)*floor(prefix_len/page_size)
+ * pages.  Writes block_table (host, [batch, max_pages], unused entries -1) and
+ * *pages_used (nullable) = fresh pages taken.  INVALID if a request needs
+ * more than max_pages pages or a length is negative; OOM if the pool runs
+ * out.  On any error every page this call took is returned and the table is
+ * all -1. */
+pks_status pks_build_block_table(pks_pool* pool, int32_t batch, const int32_t* seq_lens,
+                                 const int32_t* prefix_group, int32_t prefix_len,
+                                 int32_t max_pages, int32_t* block_table, int32_t* pages_used);
+
+/* ------------------------------------------------------------------------
+ * Decode step ([SA] introduction and DeepSeek Sparse Attention paragraph).
+ *
+ * For every request b with len_b = seq_lens[b]:
+ *  1. indexer scan: s[b,t] = sum_h w_idx[h] * max(0, q_idx[b,h,:] . k_idx(b,t)) in
+ *     int32 for every t < len_b, k_idx(b,t) = idx_k[block_table[b][t/page_size],
+ *     t % page_size, :].  The caller keeps sum_h |w_idx[h]| * Di * 128^2 < 2^31.
+ *  2. top-k: if len_b <= k all tokens (dense); else the k tokens first in the
+ *     order (score descending, token index ascending).  Written to topk_idx in
+ *     ascending token order, -1 padded.
+ *  3. attention: out[b,h] = softmax(q[b,h] . K_sel / sqrt(D)) V_sel over the
+ *     selected tokens, K/V rows gathered through block_table; bf16 inputs,
+ *     fp32 accumulation, bf16 output.  A request with len_b = 0 gets zeros.
+ *
+ * Compiled shapes (else UNSUPPORTED): D in {64, 128}; Di in {64, 128};
+ * Hi in {1, 2, 4, 8}; 1 <= Hq/Hkv <= 16; B <= 4096; k <= 65536;
+ * max_pages*page_size <= 2^24.  q, kv_k, kv_v, q_idx, idx_k must be 16-byte
+ * aligned (INVALID otherwise).
+ * ---------------------------------------------------------------------- */
+typedef struct pks_decode_args {
+  int32_t B, Hq, Hkv, D, Hi, Di;
+  int32_t page_size, max_pages, num_pages, k;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  const void* q;
+  const int8_t* q_idx;
+  const int32_t* w_idx;
+  const void* kv_k;
+  const void* kv_v;
+  const int8_t* idx_k;
+  int32_t* topk_idx;      /* output of the step; input of pks_sparse_attention */
+  void* out;
+  void* workspace;        /* device scratch owned by the caller, 256-byte aligned */
+  size_t workspace_bytes;
+  int32_t attn_splits;    /* 0 = choose; else split each request's k tokens this many ways */
+  int32_t reserved[3];    /* must be 0 */
+} pks_decode_args;
+
+/* Workspace bytes a step with these shapes needs (pointers may be NULL). */
+pks_status pks_decode_workspace_size(const pks_decode_args* args, size_t* bytes);
+
+/* Zero the workspace's control words.  Required once before the first step on
+ * a workspace (or zero the whole buffer with cudaMemset); every completed step
+ * leaves them zero again, so steps can be replayed (e.g. in a CUDA graph). */
+pks_status pks_decode_workspace_init(const pks_decode_args* args, pks_stream stream);
+
+/* The whole step: scan, top-k, attention.  Four kernel launches. */
+pks_status pks_decode_step(const pks_decode_args* args, pks_stream stream);
+
+/* Same as pks_decode_step, recording events[0..3] (nullable entries) before the
+ * scan, after the scan, after the top-k kernels and after attention. */
+pks_status pks_decode_step_timed(const pks_decode_args* args, pks_stream stream,
+                                 pks_event const* events);
+
+/* Stage 1 alone, for inspection: int32 scores into scores[b * ld + t] for
+ * t < len_b (device; ld >= max_pages*page_size); other entries untouched.
+ * Uses no workspace. */
+pks_status pks_indexer_scores(const pks_decode_args* args, int32_t* scores, int64_t ld,
+                              pks_stream stream);
+
+/* Stage 3 alone: attention over the tokens the caller put in args->topk_idx
+ * (any order, -1 entries skipped, each position must be < len_b).  Writes
+ * args->out; uses the workspace. */
+pks_status pks_sparse_attention(const pks_decode_args* args, pks_stream stream);
+
+/* Copy the workspace's device error word to *code (host) and clear it;
+ * synchronises the stream.  *code = 0 when no device check fired, else the
+ * PKS_ERR_DEVICE_CHECK cause: 1 page id out of [0, num_pages), 2 selected
+ * token position outside [0, len_b), 3 sequence length outside
+ * [0, max_pages*page_size]. */
+pks_status pks_decode_device_error(const pks_decode_args* args, int32_t* code,
+                                   pks_stream stream);
+
+/* ------------------------------------------------------------------------
+ * HBM residency table ([SA] HiSparse paragraph).  A table of `capacity`
+ * slots over physical pages [0, num_pages), kept in one caller-owned device
+ * buffer (`state`, 256-byte aligned) with this layout (int32 unless noted):
+ *   [0..15]                header: num_pages, capacity, step, n_resident,
+ *                          device error word, magic, reserved
+ *   page_slot[num_pages]   slot of a resident page, -1 otherwise
+ *   slot_page[capacity]    page held by a slot, -1 if empty
+ *   last_use[capacity]     step of the slot's last use, -1 if never
+ *   lru_order[capacity]    slots ordered by (last_use ascending, slot ascending)
+ *   scratch (flags and a victim list), zero between calls
+ * Each section starts on a 256-byte boundary; pks_residency_offsets gives them.
+ * ---------------------------------------------------------------------- */
+pks_status pks_residency_state_bytes(int32_t num_pages, int32_t capacity, size_t* bytes);
+
+/* Byte offsets of page_slot, slot_page, last_use and lru_order inside the state. */
+pks_status pks_residency_offsets(int32_t num_pages, int32_t capacity, size_t* page_slot,
+                                 size_t* slot_page, size_t* last_use, size_t* lru_order);
+
+/* Fill `state`: the n_init distinct pages of init_pages (host) go to slots
+ * 0..n_init-1 in ascending page order with last use 0; other slots are empty.
+ * Validates on the host (INVALID on duplicates, range, n_init > capacity),
+ * then copies with cudaMemcpyAsync on `stream`. */
+pks_status pks_residency_init(void* state, int32_t num_pages, int32_t capacity,
+                              int32_t n_init, const int32_t* init_pages, pks_stream stream);
+
+/* One step.  A = distinct physical pages block_table[b][t / page_size] over
+ * every selected t = topk_idx[b][j] >= 0.  Writes miss_list[0..n) = A minus
+ * the pages resident at the start of the step, ascending, and *n_miss = n
+ * (device scalar).  Pages of A already resident get last use = step; the
+ * slots not holding a page of A are victims in (last use, slot) order, and
+ * the i-th miss takes the i-th victim's slot (last use = step).  Misses beyond
+ * the victims are reported but not admitted, so a step never evicts a page it
+ * reads.  miss_list needs num_pages entries.  Two kernel launches. */
+pks_status pks_residency_update(void* state, int32_t num_pages, int32_t capacity, int32_t B,
+                                int32_t k, int32_t page_size, int32_t max_pages,
+                                const int32_t* topk_idx, const int32_t* block_table,
+                                int32_t* miss_list, int32_t* n_miss, pks_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKS_H */

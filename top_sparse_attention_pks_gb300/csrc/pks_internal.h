@@ -1,0 +1,70 @@
+// Internal declarations shared by the host layer and the kernel files of libpks.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pks.h"
+
+namespace pks {
+
+// ---- indexer score histogram (fused into the scan, consumed by top-k) ----
+// 2048 bins over int32 scores, order preserving: 0 -> bin 1024; |s| > 0 is
+// binned by its leading-one position e (0..31) and the next 5 bits m, giving
+// 32 bins per power of two (about 2% wide); positives above 1024, negatives
+// mirrored below.
+constexpr int kScoreBins = 2048;
+// Tokens per top-k chunk (one CTA of the threshold and emit kernels).
+constexpr int kTopkChunk = 4096;
+// Attention: tokens per pipeline tile and positions per split granule.
+constexpr int kAttnTile = 64;
+
+// Device error word causes (see pks_decode_device_error).
+constexpr int kErrPage = 1;
+constexpr int kErrToken = 2;
+constexpr int kErrLen = 3;
+constexpr int kErrState = 4;
+// header word 5 of a residency state filled by pks_residency_init
+constexpr int32_t kResidencyMagic = 0x504b5352;
+
+struct TopkThreshold {
+  int32_t bin;        // coarse threshold bin T1
+  int32_t pad;
+  uint64_t key;       // exact threshold on (score, ~token) among bin-T1 tokens
+};
+
+// Byte offsets of the workspace regions for one set of shapes.  Every region
+// starts on a 256-byte boundary.  The control block (error word, histograms,
+// tickets, counters) must be zero between steps; everything else is scratch.
+struct WorkspaceLayout {
+  size_t ctrl, err, hist, tick_topk, cand_n, tick_attn, ctrl_end;
+  size_t scores, cand, gt_cnt, chunk_off, thresh, part_ml, part_o;
+  size_t total;
+  int64_t ld;          // score row stride (max_pages * page_size)
+  int32_t nchunks;     // top-k chunks per request
+  int32_t splits;      // attention splits per (request, kv head)
+  int32_t split_len;   // top-k positions per split (multiple of kAttnTile)
+};
+
+WorkspaceLayout workspace_layout(const pks_decode_args& a);
+
+// ---- kernel launchers (each returns cudaGetLastError() after launch) ----
+cudaError_t launch_indexer_scan(const pks_decode_args& a, int32_t* scores, int64_t ld,
+                                int32_t* hist, int32_t* err, cudaStream_t s);
+cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
+                        cudaStream_t s);
+cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
+                             cudaStream_t s);
+cudaError_t launch_residency(int32_t* state, int32_t num_pages, int32_t capacity, int32_t B,
+                             int32_t k, int32_t page_size, int32_t max_pages,
+                             const int32_t* topk_idx, const int32_t* block_table,
+                             int32_t* miss_list, int32_t* n_miss, size_t off_page_slot,
+                             size_t off_slot_page, size_t off_last_use, size_t off_lru,
+                             size_t off_flag, size_t off_slot_flag, size_t off_vict,
+                             cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace pks
