@@ -82,7 +82,8 @@ def test_negative_weights_and_small_range_ties():
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
 def test_attention_split_counts(splits):
-    wl = WORKLOADS["paging_example"].replace(k=256, seq_lens=(403, 300, 241, 30, 256))
+    wl = WORKLOADS["paging_example"].replace(k=256, seq_lens=(403, 300, 241, 30, 256),
+                                             num_pages=96)
     t, _, _ = prepare(wl)
     full_check(wl, t, attn_splits=splits)
 
