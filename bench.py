@@ -219,6 +219,9 @@ def main():
     ap.add_argument("--impl", default="pks", choices=["pks", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--requests", type=int, default=0,
+                    help="keep only the first N requests (smaller profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -242,6 +245,8 @@ def main():
     if dist:
         dist.barrier()
     wl = WORKLOADS[args.workload]
+    if args.requests:
+        wl = shrink(wl, args.requests)
     t, h, bt = setup(wl, dev, seed_offset=rank)
 
     if args.impl == "reference":
@@ -286,7 +291,10 @@ def main():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         one_step(s)
-    launches_per_step = 4 + (2 if res is not None else 0)
+    # scan, top-k threshold (+ top-k emit beyond 131072-token contexts),
+    # attention + merge, (+ residency mark and update)
+    launches_per_step = (4 + (1 if wl.max_pages * wl.page_size > 131072 else 0)
+                         + (2 if res is not None else 0))
 
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
@@ -385,6 +393,19 @@ def main():
         dist.destroy_process_group()
 
 
+def shrink(wl, n):
+    """The first n requests of a workload, with the pool cut to match."""
+    if n >= wl.B:
+        return wl
+    kw = dict(B=n, num_pages=max(1, wl.num_pages * n // wl.B))
+    if wl.seq_lens:
+        kw["seq_lens"] = tuple(wl.seq_lens[:n])
+    if wl.capacity:
+        kw["capacity"] = max(1, wl.capacity * n // wl.B)
+        kw["initial_resident"] = max(0, wl.initial_resident * n // wl.B)
+    return wl.replace(**kw)
+
+
 def config_dict(wl, args):
     return {"workload": wl.name, "requests": wl.B,
             "seq_len": list(wl.seq_lens) if wl.seq_lens and len(set(wl.seq_lens)) > 1
@@ -434,7 +455,7 @@ def end_to_end(step, t, wl, args, s, flush, res, miss, n_miss):
     if res is not None:
         extra = [torch.empty(1, dtype=torch.int32).pin_memory()]
         d2h += 4
-    n = min(args.steps, 500)
+    n = max(1, min(args.steps, args.e2e_steps))
     total = 0.0
     with torch.cuda.stream(s):
         for i in range(n + 3):

@@ -143,7 +143,9 @@ typedef struct pks_decode_args {
   void* out;
   void* workspace;        /* device scratch owned by the caller, 256-byte aligned */
   size_t workspace_bytes;
-  int32_t attn_splits;    /* 0 = choose; else split each request's k tokens this many ways */
+  int32_t attn_splits;    /* attention CTAs: 0 = one per resident slot on the GPU; else this
+                             many (1..1024), each taking an equal share of all selected
+                             (KV head group, request, position) work */
   int32_t reserved[3];    /* must be 0 */
 } pks_decode_args;
 
@@ -155,7 +157,8 @@ pks_status pks_decode_workspace_size(const pks_decode_args* args, size_t* bytes)
  * leaves them zero again, so steps can be replayed (e.g. in a CUDA graph). */
 pks_status pks_decode_workspace_init(const pks_decode_args* args, pks_stream stream);
 
-/* The whole step: scan, top-k, attention.  Four kernel launches. */
+/* The whole step: scan, top-k, attention.  Four kernel launches (five when
+ * max_pages*page_size exceeds 131072 tokens). */
 pks_status pks_decode_step(const pks_decode_args* args, pks_stream stream);
 
 /* Same as pks_decode_step, recording events[0..3] (nullable entries) before the

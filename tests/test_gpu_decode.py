@@ -80,7 +80,7 @@ def test_negative_weights_and_small_range_ties():
     full_check(wl, t)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64, 1000])
 def test_attention_split_counts(splits):
     wl = WORKLOADS["paging_example"].replace(k=256, seq_lens=(403, 300, 241, 30, 256),
                                              num_pages=96)
@@ -104,6 +104,16 @@ def test_ragged_prefix_reduced():
 
 def test_128k_reduced():
     wl = WORKLOADS["b16_128k"].replace(B=2, seq_lens=(131072, 131072), num_pages=4096)
+    t, _, _ = prepare(wl)
+    full_check(wl, t)
+
+
+def test_long_request_emit_path():
+    # a context longer than the top-k bitmap (131072 tokens) goes through the
+    # chunked emit kernel; a second, short request keeps the bitmap path
+    wl = WORKLOADS["paging_example"].replace(
+        B=2, seq_lens=(140000, 5000), page_size=64, max_pages=2200, num_pages=2300, k=512,
+        Di=64, D=64, Hq=8, Hkv=2)
     t, _, _ = prepare(wl)
     full_check(wl, t)
 

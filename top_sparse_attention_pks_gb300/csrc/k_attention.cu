@@ -30,8 +30,8 @@
 namespace pks {
 namespace {
 
-constexpr int kAttnThreads = 128;
-constexpr int kStages = 3;
+constexpr int kAttnStages = 3;      // shared-memory ring depth in tiles
+constexpr int kAttnRowCap = 2048;   // positions whose rows are resolved at once
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -79,60 +79,130 @@ __device__ __forceinline__ void flag_error(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 2)
+// Decode flattened position f (head group major, then request, then top-k
+// position) of a CTA's range into its segment (group, request) and position.
+struct SegCursor {
+  int g, b, p;      // head group, request, position within the request's list
+  int seg_end;      // flattened end of the current segment
+};
+
+__device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// CTA that owns flattened position f when [0, T) is cut into G equal ranges.
+__device__ __forceinline__ int owner_cta(int64_t f, int64_t T, int64_t G) {
+  return (int)(((f + 1) * G + T - 1) / T - 1);
+}
+
+template <int D, int HG>
+__global__ void __launch_bounds__(HG * 32, 1)
 k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv_k,
                    const __nv_bfloat16* __restrict__ kv_v, const int32_t* __restrict__ topk,
-                   int32_t* __restrict__ tick, float2* __restrict__ part_ml,
+                   int32_t* __restrict__ prefix_out, float2* __restrict__ part_ml,
                    float* __restrict__ part_o, __nv_bfloat16* __restrict__ out,
-                   int32_t* __restrict__ err, int Hq, int Hkv, int G, int page_size,
-                   int max_pages, int num_pages, int k, int split_len, float scale_log2) {
-  constexpr int CH = D / 8;   // 16-byte chunks per row
+                   int32_t* __restrict__ err, int B, int Hq, int Hkv, int G, int page_size,
+                   int max_pages, int num_pages, int k, int trim, float scale_log2) {
+  constexpr int NT = HG * 32;
+  constexpr int CH = D / 8;   // 16-byte chunks per head row
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int ND = D / 8;   // 8-wide column tiles of O
   constexpr int TILE = kAttnTile;
+  constexpr int STAGE_ELEMS = TILE * HG * D;  // one of K or V
   const float kNegInf = __int_as_float(0xff800000);
 
   extern __shared__ __align__(128) uint8_t smem[];
-  int32_t* s_row = reinterpret_cast<int32_t*>(smem);
-  const int row_bytes = (split_len * 4 + 127) & ~127;
-  __nv_bfloat16* s_kv = reinterpret_cast<__nv_bfloat16*>(smem + row_bytes);
-  __shared__ int s_last;
+  __nv_bfloat16* s_kv = reinterpret_cast<__nv_bfloat16*>(smem);  // [stages][K|V][TILE][HG][D]
+  int32_t* s_row = reinterpret_cast<int32_t*>(smem + (size_t)kAttnStages * 2 * STAGE_ELEMS * 2);
+  int32_t* s_prefix = s_row + kAttnRowCap;  // [B + 1] top-k positions per request, prefix
+  __shared__ int s_warp[NT / 32];
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z, splits = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int max_len = max_pages * page_size;
-  int len = seq_lens[b];
-  if (len < 0 || len > max_len) {
-    if (h == 0 && split == 0 && tid == 0) flag_error(err, kErrLen);
-    len = 0;
-  }
-  const int p0 = split * split_len;
-  const int n_pos = max(0, min(k, p0 + split_len) - p0);
+  const int ngroups = Hkv / HG;
 
-  // ---- selected positions -> physical token rows (page * page_size + slot)
-  const int32_t* bt = block_table + (int64_t)b * max_pages;
-  for (int i = tid; i < n_pos; i += kAttnThreads) {
-    const int t = topk[(int64_t)b * k + p0 + i];
-    int row = -1;
-    if (t >= 0) {
-      if (t >= len) {
-        flag_error(err, kErrToken);
-      } else {
-        const int page = bt[t / page_size];
-        if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
-        else flag_error(err, kErrPage);
+  // ---- prefix over requests of the positions to visit: k_b = min(k, len_b)
+  // when the list is the step's own top-k (selected entries first, -1 after),
+  // else all k positions (entries may sit anywhere)
+  {
+    const int per = (B + NT - 1) / NT;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b < B) {
+        const int len = seq_lens[b];
+        local += (len < 0 || len > max_len) ? 0 : (trim ? min(len, k) : k);
       }
     }
-    s_row[i] = row;
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    int before = x - local;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b < B) {
+        s_prefix[b] = before;
+        const int len = seq_lens[b];
+        before += (len < 0 || len > max_len) ? 0 : (trim ? min(len, k) : k);
+      }
+    }
+    if (tid == NT - 1) s_prefix[B] = before;
+    __syncthreads();
   }
+  const int64_t Treq = s_prefix[B];
+  const int64_t T = Treq * ngroups;
+  // with fewer positions than CTAs only the first T CTAs take part, so every
+  // participating CTA owns at least one position and the contributors of a
+  // segment are exactly the CTAs from its first to its last owner
+  const int64_t GRID = T < (int64_t)gridDim.x ? T : (int64_t)gridDim.x;
+  const int cta = blockIdx.x;
 
-  // ---- Q fragments of the G heads (rows >= G are zero)
+  // requests with no position to visit (length 0) get zero outputs; CTA 0
+  // also publishes the position prefix for the merge kernel
+  if (cta == 0) {
+    for (int i = tid; i <= B; i += NT) prefix_out[i] = s_prefix[i];
+    for (int b = 0; b < B; ++b) {
+      if (s_prefix[b + 1] != s_prefix[b]) continue;
+      for (int i = tid; i < Hq * D; i += NT) out[(int64_t)b * Hq * D + i] = __float2bfloat16(0.f);
+    }
+  }
+  if (T == 0 || cta >= GRID) return;
+  const int64_t lo = cta * T / GRID, hi = (cta + 1) * T / GRID;
+  if (lo >= hi) return;
+
+  auto locate = [&](int64_t f) {
+    SegCursor c;
+    c.g = (int)(f / Treq);
+    const int fb = (int)(f - (int64_t)c.g * Treq);
+    int l = 0, h = B - 1;  // last request with prefix <= fb
+    while (l < h) {
+      const int mid = (l + h + 1) >> 1;
+      if (s_prefix[mid] <= fb) l = mid; else h = mid - 1;
+    }
+    c.b = l;
+    c.p = fb - s_prefix[l];
+    c.seg_end = (int)((int64_t)c.g * Treq + s_prefix[l + 1]);
+    return c;
+  };
+
   const int ra = lane >> 2, rb = ra + 8, cq = (lane & 3) * 2;
   uint32_t qa[KS][4];
-  {
-    const __nv_bfloat16* qb = q + ((int64_t)b * Hq + (int64_t)h * G) * D;
+  float o[ND][4];
+  float m_a, m_b, l_a, l_b;
+  auto reset_state = [&]() {
+#pragma unroll
+    for (int i = 0; i < ND; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    m_a = m_b = kNegInf;
+    l_a = l_b = 0.f;
+  };
+  auto load_q = [&](int g, int b) {
+    const int head = g * HG + warp;  // this warp's KV head
+    const __nv_bfloat16* qb = q + ((int64_t)b * Hq + (int64_t)head * G) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const int col = ks * 16 + cq;
@@ -141,209 +211,311 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
       qa[ks][2] = ra < G ? *reinterpret_cast<const uint32_t*>(qb + ra * D + col + 8) : 0u;
       qa[ks][3] = rb < G ? *reinterpret_cast<const uint32_t*>(qb + rb * D + col + 8) : 0u;
     }
-  }
-  __syncthreads();
+  };
 
-  const int n_tiles = (n_pos + TILE - 1) / TILE;
-  auto load_tile = [&](int tile, int stage) {
-    __nv_bfloat16* sk = s_kv + (size_t)stage * 2 * TILE * D;
-    __nv_bfloat16* sv = sk + TILE * D;
-#pragma unroll 4
-    for (int idx = tid; idx < TILE * CH; idx += kAttnThreads) {
-      const int r = idx / CH, c = idx % CH;
-      const int pos = tile * TILE + r;
-      const int row = pos < n_pos ? s_row[pos] : -1;
-      const int off = r * D + ((c ^ (r & 7)) << 3);
-      const int64_t src = row >= 0 ? ((int64_t)row * Hkv + h) * D + c * 8 : 0;
-      const int bytes = row >= 0 ? 16 : 0;  // 0 bytes: zero fill
-      cp_async16(smem_u32(sk + off), kv_k + src, bytes);
-      cp_async16(smem_u32(sv + off), kv_v + src, bytes);
+  // write this CTA's share of segment (g, b): the whole output when it owns
+  // the whole segment, else a partial (m, l, o) that k_attention_merge combines
+  auto finish_segment = [&](int g, int b, int64_t seg_lo, int64_t seg_hi) {
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    const int head = g * HG + warp;
+    const int c_first = owner_cta(seg_lo, T, GRID), c_last = owner_cta(seg_hi - 1, T, GRID);
+    __nv_bfloat16* ob = out + ((int64_t)b * Hq + (int64_t)head * G) * D;
+    if (c_first == c_last) {
+      const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        const int d = nd * 8 + cq;
+        if (ra < G)
+          *reinterpret_cast<__nv_bfloat162*>(ob + ra * D + d) =
+              __floats2bfloat162_rn(o[nd][0] * ia, o[nd][1] * ia);
+        if (rb < G)
+          *reinterpret_cast<__nv_bfloat162*>(ob + rb * D + d) =
+              __floats2bfloat162_rn(o[nd][2] * ib, o[nd][3] * ib);
+      }
+      return;
+    }
+    const int seg = g * B + b;
+    const int64_t slot = (int64_t)cta + seg;
+    const int64_t base = (slot * HG + warp) * G;
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) {
+      const int d = nd * 8 + cq;
+      if (ra < G) *reinterpret_cast<float2*>(part_o + (base + ra) * D + d) = make_float2(o[nd][0], o[nd][1]);
+      if (rb < G) *reinterpret_cast<float2*>(part_o + (base + rb) * D + d) = make_float2(o[nd][2], o[nd][3]);
+    }
+    if ((lane & 3) == 0) {
+      if (ra < G) part_ml[base + ra] = make_float2(m_a, l_a);
+      if (rb < G) part_ml[base + rb] = make_float2(m_b, l_b);
     }
   };
 
-  float o[ND][4];
-#pragma unroll
-  for (int i = 0; i < ND; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
+  // consumer cursor: segment whose state the warps hold
+  int64_t cs_pos = lo;
+  SegCursor csc{0, 0, 0, 0};
+  bool have_state = false;
+  for (int64_t chunk_lo = lo; chunk_lo < hi; chunk_lo += kAttnRowCap) {
+    const int64_t chunk_hi = lmin(hi, chunk_lo + kAttnRowCap);
+    // ---- physical token rows of the chunk's positions: those of the first
+    // tiles first, so their copies start while the rest are looked up
+    auto resolve_rows = [&](int64_t f0, int64_t f1) {
+      for (int64_t f = f0 + tid; f < f1; f += NT) {
+        const SegCursor c = locate(f);
+        int len = seq_lens[c.b];
+        if (len < 0 || len > max_len) len = 0;
+        const int t = topk[(int64_t)c.b * k + c.p];
+        int row = -1;
+        if (t >= 0) {
+          if (t >= len) {
+            flag_error(err, kErrToken);
+          } else {
+            const int page = block_table[(int64_t)c.b * max_pages + t / page_size];
+            if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
+            else flag_error(err, kErrPage);
+          }
+        }
+        s_row[f - chunk_lo] = row;
+      }
+    };
+    const int64_t early_hi = lmin(chunk_hi, chunk_lo + (int64_t)(kAttnStages - 1) * TILE);
+    resolve_rows(chunk_lo, early_hi);
+    __syncthreads();
 
-#pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
-    if (st < n_tiles) load_tile(st, st);
-    cp_async_commit();
-  }
+    // ---- tiles: runs of up to TILE positions inside one segment
+    int64_t ld_pos = chunk_lo;  // flattened position of the next tile to load
+    int ld_seg_end = locate(chunk_lo).seg_end;
+    auto load_next = [&](int stage) {
+      if (ld_pos >= chunk_hi) return;
+      if (ld_pos >= ld_seg_end) ld_seg_end = locate(ld_pos).seg_end;
+      const int n = (int)lmin(TILE, lmin(ld_seg_end, chunk_hi) - ld_pos);
+      const int g = (int)(ld_pos / Treq);
+      __nv_bfloat16* sk = s_kv + (size_t)stage * 2 * STAGE_ELEMS;
+      __nv_bfloat16* sv = sk + STAGE_ELEMS;
+      const int rbase = (int)(ld_pos - chunk_lo);
+#pragma unroll 4
+      for (int idx = tid; idx < TILE * HG * CH; idx += NT) {
+        const int r = idx / (HG * CH), rem = idx % (HG * CH);
+        const int hh = rem / CH, c = rem % CH;
+        const int row = r < n ? s_row[rbase + r] : -1;
+        const int off = (r * HG + hh) * D + ((c ^ (r & 7)) << 3);
+        const int64_t src = row >= 0 ? ((int64_t)row * Hkv + g * HG + hh) * D + c * 8 : 0;
+        const int bytes = row >= 0 ? 16 : 0;  // 0 bytes: zero fill
+        cp_async16(smem_u32(sk + off), kv_k + src, bytes);
+        cp_async16(smem_u32(sv + off), kv_v + src, bytes);
+      }
+      ld_pos += n;
+    };
 
-  const int r0 = warp * 16;
-  for (int tile = 0; tile < n_tiles; ++tile) {
+    int n_tiles = 0;
     {
-      const int nt = tile + kStages - 1;
-      if (nt < n_tiles) load_tile(nt, nt % kStages);
+      // count tiles of the chunk (uniform across the CTA)
+      int64_t f = chunk_lo;
+      int se = ld_seg_end;
+      while (f < chunk_hi) {
+        if (f >= se) se = locate(f).seg_end;
+        f += lmin(TILE, lmin(se, chunk_hi) - f);
+        ++n_tiles;
+      }
+    }
+#pragma unroll
+    for (int st = 0; st < kAttnStages - 1; ++st) {
+      if (st < n_tiles) load_next(st);
       cp_async_commit();
     }
-    cp_async_wait<kStages - 1>();
+    resolve_rows(early_hi, chunk_hi);
     __syncthreads();
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      if (tile + kAttnStages - 1 < n_tiles) load_next((tile + kAttnStages - 1) % kAttnStages);
+      cp_async_commit();
+      if (!have_state || cs_pos >= csc.seg_end) {
+        csc = locate(cs_pos);
+        load_q(csc.g, csc.b);
+        reset_state();
+        have_state = true;
+      }
+      const int n = (int)lmin(TILE, lmin(csc.seg_end, chunk_hi) - cs_pos);
+      const int rbase = (int)(cs_pos - chunk_lo);
+      cp_async_wait<kAttnStages - 1>();
+      __syncthreads();
 
-    const __nv_bfloat16* sk = s_kv + (size_t)(tile % kStages) * 2 * TILE * D;
-    const __nv_bfloat16* sv = sk + TILE * D;
-
-    // S^T fragments: 16 heads (rows) x 16 tokens (2 column tiles)
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const __nv_bfloat16* sk = s_kv + (size_t)(tile % kAttnStages) * 2 * STAGE_ELEMS;
+      const __nv_bfloat16* sv = sk + STAGE_ELEMS;
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int row = r0 + ((lane >> 4) << 3) + (lane & 7);
-      const int chunk = 2 * ks + ((lane >> 3) & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(smem_u32(sk + row * D + ((chunk ^ (row & 7)) << 3)), b0, b1, b2, b3);
-      mma_bf16(sacc[0], qa[ks], b0, b1);
-      mma_bf16(sacc[1], qa[ks], b2, b3);
-    }
-
-    // online softmax (log2 domain) for rows ra and rb
-    float x[2][4];
+      for (int ks = 0; ks < KS; ++ks) {
+        const int row = ((lane >> 4) << 3) + (lane & 7);
+        const int chunk = 2 * ks + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(sk + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), b0, b1, b2, b3);
+        mma_bf16(sacc[0], qa[ks], b0, b1);
+        mma_bf16(sacc[1], qa[ks], b2, b3);
+      }
+      float x[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int pos = tile * TILE + r0 + nt * 8 + cq + e;
-        const bool valid = pos < n_pos && s_row[pos] >= 0;
-        x[nt][e] = valid ? sacc[nt][e] * scale_log2 : kNegInf;
-        x[nt][e + 2] = valid ? sacc[nt][e + 2] * scale_log2 : kNegInf;
+        for (int e = 0; e < 2; ++e) {
+          const int r = nt * 8 + cq + e;
+          const bool valid = r < n && s_row[rbase + r] >= 0;
+          x[nt][e] = valid ? sacc[nt][e] * scale_log2 : kNegInf;
+          x[nt][e + 2] = valid ? sacc[nt][e + 2] * scale_log2 : kNegInf;
+        }
+      }
+      float mx_a = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      float mx_b = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+      const float al_a = mn_a == kNegInf ? 1.f : exp2f(m_a - mn_a);
+      const float al_b = mn_b == kNegInf ? 1.f : exp2f(m_b - mn_b);
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        p[nt][0] = x[nt][0] == kNegInf ? 0.f : exp2f(x[nt][0] - mn_a);
+        p[nt][1] = x[nt][1] == kNegInf ? 0.f : exp2f(x[nt][1] - mn_a);
+        p[nt][2] = x[nt][2] == kNegInf ? 0.f : exp2f(x[nt][2] - mn_b);
+        p[nt][3] = x[nt][3] == kNegInf ? 0.f : exp2f(x[nt][3] - mn_b);
+      }
+      l_a = l_a * al_a + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+      l_b = l_b * al_b + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+      m_a = mn_a;
+      m_b = mn_b;
+#pragma unroll
+      for (int i = 0; i < ND; ++i) {
+        o[i][0] *= al_a;
+        o[i][1] *= al_a;
+        o[i][2] *= al_b;
+        o[i][3] *= al_b;
+      }
+      const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]),
+                              pack_bf16(p[1][0], p[1][1]), pack_bf16(p[1][2], p[1][3])};
+#pragma unroll
+      for (int nd = 0; nd < ND; nd += 2) {
+        const int row = (((lane >> 3) & 1) << 3) + (lane & 7);
+        const int chunk = nd + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_u32(sv + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), b0, b1, b2, b3);
+        mma_bf16(o[nd], pa, b0, b1);
+        mma_bf16(o[nd + 1], pa, b2, b3);
+      }
+      __syncthreads();
+      cs_pos += n;
+      if (cs_pos == csc.seg_end || cs_pos == hi) {
+        const int64_t seg_lo = (int64_t)csc.g * Treq + s_prefix[csc.b];
+        finish_segment(csc.g, csc.b, seg_lo, csc.seg_end);
+        have_state = false;
       }
     }
-    float mx_a = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-    float mx_b = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-    const float al_a = mn_a == kNegInf ? 1.f : exp2f(m_a - mn_a);
-    const float al_b = mn_b == kNegInf ? 1.f : exp2f(m_b - mn_b);
-    float p[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      p[nt][0] = x[nt][0] == kNegInf ? 0.f : exp2f(x[nt][0] - mn_a);
-      p[nt][1] = x[nt][1] == kNegInf ? 0.f : exp2f(x[nt][1] - mn_a);
-      p[nt][2] = x[nt][2] == kNegInf ? 0.f : exp2f(x[nt][2] - mn_b);
-      p[nt][3] = x[nt][3] == kNegInf ? 0.f : exp2f(x[nt][3] - mn_b);
-    }
-    l_a = l_a * al_a + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-    l_b = l_b * al_b + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-    m_a = mn_a;
-    m_b = mn_b;
-#pragma unroll
-    for (int i = 0; i < ND; ++i) {
-      o[i][0] *= al_a;
-      o[i][1] *= al_a;
-      o[i][2] *= al_b;
-      o[i][3] *= al_b;
-    }
-    const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]),
-                            pack_bf16(p[1][0], p[1][1]), pack_bf16(p[1][2], p[1][3])};
-#pragma unroll
-    for (int nd = 0; nd < ND; nd += 2) {
-      const int row = r0 + (((lane >> 3) & 1) << 3) + (lane & 7);
-      const int chunk = nd + (lane >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(smem_u32(sv + row * D + ((chunk ^ (row & 7)) << 3)), b0, b1, b2, b3);
-      mma_bf16(o[nd], pa, b0, b1);
-      mma_bf16(o[nd + 1], pa, b2, b3);
-    }
+    cp_async_wait<0>();
     __syncthreads();
   }
-  cp_async_wait<0>();
-  __syncthreads();
-
-  // ---- merge the 4 warps' states in shared memory (reusing the ring)
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  float* s_o = reinterpret_cast<float*>(s_kv);  // [4][16][D]
-  float* s_m = s_o + 4 * 16 * D;                // [4][16]
-  float* s_l = s_m + 4 * 16;                    // [4][16]
-#pragma unroll
-  for (int nd = 0; nd < ND; ++nd) {
-    const int d = nd * 8 + cq;
-    s_o[(warp * 16 + ra) * D + d] = o[nd][0];
-    s_o[(warp * 16 + ra) * D + d + 1] = o[nd][1];
-    s_o[(warp * 16 + rb) * D + d] = o[nd][2];
-    s_o[(warp * 16 + rb) * D + d + 1] = o[nd][3];
-  }
-  if ((lane & 3) == 0) {
-    s_m[warp * 16 + ra] = m_a;
-    s_l[warp * 16 + ra] = l_a;
-    s_m[warp * 16 + rb] = m_b;
-    s_l[warp * 16 + rb] = l_b;
-  }
-  __syncthreads();
-
-  const int64_t bh = (int64_t)b * Hkv + h;
-  for (int idx = tid; idx < G * D; idx += kAttnThreads) {
-    const int g = idx / D, d = idx % D;
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, s_m[w * 16 + g]);
-    float L = 0.f, O = 0.f;
-    if (M != kNegInf) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float mw = s_m[w * 16 + g];
-        if (mw == kNegInf) continue;
-        const float f = exp2f(mw - M);
-        L += s_l[w * 16 + g] * f;
-        O += s_o[(w * 16 + g) * D + d] * f;
-      }
-    }
-    if (splits == 1) {
-      out[((int64_t)b * Hq + (int64_t)h * G + g) * D + d] = __float2bfloat16(L > 0.f ? O / L : 0.f);
-    } else {
-      const int64_t slot = (bh * splits + split) * G + g;
-      part_o[slot * D + d] = O;
-      if (d == 0) part_ml[slot] = make_float2(M, L);
-    }
-  }
-  if (splits == 1) return;
-
-  // ---- the last split CTA of (request, KV head) merges the splits
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(tick + bh, 1) == splits - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int idx = tid; idx < G * D; idx += kAttnThreads) {
-    const int g = idx / D, d = idx % D;
-    float M = kNegInf;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(&part_ml[(bh * splits + s) * G + g].x));
-    float L = 0.f, O = 0.f;
-    if (M != kNegInf) {
-      for (int s = 0; s < splits; ++s) {
-        const int64_t slot = (bh * splits + s) * G + g;
-        const float2 ml = __ldcg(&part_ml[slot]);
-        if (ml.x == kNegInf) continue;
-        const float f = exp2f(ml.x - M);
-        L += ml.y * f;
-        O += __ldcg(&part_o[slot * D + d]) * f;
-      }
-    }
-    out[((int64_t)b * Hq + (int64_t)h * G + g) * D + d] = __float2bfloat16(L > 0.f ? O / L : 0.f);
-  }
-  if (tid == 0) tick[bh] = 0;
 }
 
+// Combine the partial (m, l, o) of a segment's contributing CTAs: one CTA per
+// (KV head, request); segments one attention CTA owned whole are skipped (it
+// wrote the output itself).  Step 1: per query row, the max and 1/sum over the
+// contributors (lanes split the contributors, warps split the rows).
+// Step 2: threads own float4 columns; contributors are read four at a time.
 template <int D>
+__global__ void __launch_bounds__(128)
+k_attention_merge(const int32_t* __restrict__ prefix, const float2* __restrict__ part_ml,
+                  const float* __restrict__ part_o, __nv_bfloat16* __restrict__ out, int B,
+                  int Hq, int Hkv, int HG, int G, int attn_grid) {
+  __shared__ float s_m[16], s_il[16];
+  const float kNegInf = __int_as_float(0xff800000);
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = h / HG, hh = h % HG;
+  const int64_t Treq = prefix[B];
+  const int64_t T = Treq * (Hkv / HG);
+  const int kb = prefix[b + 1] - prefix[b];
+  if (T == 0 || kb == 0) return;
+  const int64_t GRID = T < (int64_t)attn_grid ? T : (int64_t)attn_grid;
+  const int64_t seg_lo = (int64_t)g * Treq + prefix[b];
+  const int c_first = owner_cta(seg_lo, T, GRID), c_last = owner_cta(seg_lo + kb - 1, T, GRID);
+  if (c_first == c_last) return;
+  const int seg = g * B + b;
+  const int64_t pstride = (int64_t)HG * G;
+  // partial of contributor c, row gg: index (c + seg) * pstride + hh * G + gg
+  auto pidx = [&](int c, int gg) { return ((int64_t)c + seg) * pstride + (int64_t)hh * G + gg; };
+
+  for (int gg = warp; gg < G; gg += 4) {
+    float M = kNegInf;
+    for (int c = c_first + lane; c <= c_last; c += 32) M = fmaxf(M, __ldcg(&part_ml[pidx(c, gg)].x));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    if (M != kNegInf)
+      for (int c = c_first + lane; c <= c_last; c += 32) {
+        const float2 ml = __ldcg(&part_ml[pidx(c, gg)]);
+        if (ml.x != kNegInf) L += ml.y * exp2f(ml.x - M);
+      }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+      s_m[gg] = M;
+      s_il[gg] = L > 0.f ? 1.f / L : 0.f;
+    }
+  }
+  __syncthreads();
+
+  constexpr int DV4 = D / 4;
+  for (int it = tid; it < G * DV4; it += 128) {
+    const int gg = it / DV4, c4 = it % DV4;
+    const float M = s_m[gg];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int c = c_first;
+    for (; c + 3 <= c_last; c += 4) {
+      float m[4];
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        m[u] = __ldcg(&part_ml[pidx(c + u, gg)].x);
+        v[u] = __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c + u, gg) * D) + c4);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float f = m[u] == kNegInf ? 0.f : exp2f(m[u] - M);
+        acc.x += f * v[u].x;
+        acc.y += f * v[u].y;
+        acc.z += f * v[u].z;
+        acc.w += f * v[u].w;
+      }
+    }
+    for (; c <= c_last; ++c) {
+      const float mu = __ldcg(&part_ml[pidx(c, gg)].x);
+      const float4 vu = __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c, gg) * D) + c4);
+      const float f = mu == kNegInf ? 0.f : exp2f(mu - M);
+      acc.x += f * vu.x;
+      acc.y += f * vu.y;
+      acc.z += f * vu.z;
+      acc.w += f * vu.w;
+    }
+    const float il = s_il[gg];
+    __nv_bfloat16* dst = out + ((int64_t)b * Hq + (int64_t)h * G + gg) * D + c4 * 4;
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * il, acc.y * il);
+    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * il, acc.w * il);
+  }
+}
+
+template <int D, int HG>
+size_t attn_smem_bytes(int B) {
+  return (size_t)kAttnStages * 2 * kAttnTile * HG * D * sizeof(__nv_bfloat16) +
+         sizeof(int32_t) * (size_t)(kAttnRowCap + B + 1);
+}
+
+template <int D, int HG>
 cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
-                          cudaStream_t s) {
-  auto kern = k_sparse_attention<D>;
-  const size_t row_bytes = ((size_t)L.split_len * 4 + 127) & ~(size_t)127;
-  const size_t ring = (size_t)kStages * 2 * kAttnTile * D * sizeof(__nv_bfloat16);
-  const size_t merge = (4 * 16 * D + 2 * 4 * 16) * sizeof(float);
-  const size_t smem = row_bytes + (ring > merge ? ring : merge);
+                          bool trim, cudaStream_t s) {
+  auto kern = k_sparse_attention<D, HG>;
+  const size_t smem = attn_smem_bytes<D, HG>(a.B);
   // raise the dynamic shared-memory limit once per device and size (not a
   // stream operation, so it stays out of any graph capture after the first call)
   static size_t configured[64] = {0};
+  static int per_sm[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   size_t& done = configured[dev & 63];
@@ -352,26 +524,46 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     done = smem;
+    int bps = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, HG * 32, smem);
+    per_sm[dev & 63] = bps < 1 ? 1 : bps;
   }
+  int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * per_sm[dev & 63];
+  if (grid > L.attn_grid_max) grid = L.attn_grid_max;
   const int G = a.Hq / a.Hkv;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
-  dim3 grid(L.splits, a.Hkv, a.B);
-  kern<<<grid, kAttnThreads, smem, s>>>(
+  kern<<<grid, HG * 32, smem, s>>>(
       a.seq_lens, a.block_table, reinterpret_cast<const __nv_bfloat16*>(a.q),
       reinterpret_cast<const __nv_bfloat16*>(a.kv_k), reinterpret_cast<const __nv_bfloat16*>(a.kv_v),
-      a.topk_idx, reinterpret_cast<int32_t*>(ws + L.tick_attn),
+      a.topk_idx, reinterpret_cast<int32_t*>(ws + L.attn_prefix),
       reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
-      reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.Hq, a.Hkv,
-      G, a.page_size, a.max_pages, a.num_pages, a.k, L.split_len, scale_log2);
+      reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.B, a.Hq,
+      a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, trim ? 1 : 0, scale_log2);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_attention_merge<D><<<dim3(a.Hkv, a.B), 128, 0, s>>>(
+      reinterpret_cast<const int32_t*>(ws + L.attn_prefix),
+      reinterpret_cast<const float2*>(ws + L.part_ml), reinterpret_cast<const float*>(ws + L.part_o),
+      reinterpret_cast<__nv_bfloat16*>(a.out), a.B, a.Hq, a.Hkv, HG, G, grid);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
-                             cudaStream_t s) {
-  if (a.D == 64) return launch_attn_t<64>(a, L, ws, s);
-  if (a.D == 128) return launch_attn_t<128>(a, L, ws, s);
+                             bool trim, cudaStream_t s) {
+  const int hg = attn_heads_per_cta(a.Hkv);
+#define PKS_ATTN_CASE(D_, HG_) \
+  if (a.D == D_ && hg == HG_) return launch_attn_t<D_, HG_>(a, L, ws, trim, s);
+  PKS_ATTN_CASE(64, 1)
+  PKS_ATTN_CASE(64, 2)
+  PKS_ATTN_CASE(64, 4)
+  PKS_ATTN_CASE(64, 8)
+  PKS_ATTN_CASE(128, 1)
+  PKS_ATTN_CASE(128, 2)
+  PKS_ATTN_CASE(128, 4)
+  PKS_ATTN_CASE(128, 8)
+#undef PKS_ATTN_CASE
   return cudaErrorInvalidValue;
 }
 

@@ -34,9 +34,6 @@ constexpr size_t kAlign = 256;
 constexpr int kMaxB = 4096;
 constexpr int kMaxK = 65536;
 constexpr int64_t kMaxLen = int64_t(1) << 24;
-constexpr int kMaxSplitLen = 4096;
-// Target number of attention CTAs: 152 SMs x 2 resident CTAs x 4 waves.
-constexpr int kAttnTargetCtas = 152 * 2 * 4;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -48,7 +45,7 @@ pks_status check_shapes(const pks_decode_args* a) {
   if (!a) return PKS_ERR_INVALID;
   if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->D < 1 || a->Hi < 1 || a->Di < 1 ||
       a->page_size < 1 || a->max_pages < 1 || a->num_pages < 1 || a->k < 1 ||
-      a->attn_splits < 0)
+      a->attn_splits < 0 || a->attn_splits > kAttnGridMax)
     return PKS_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return PKS_ERR_INVALID;
   if (a->reserved[0] || a->reserved[1] || a->reserved[2]) return PKS_ERR_INVALID;
@@ -100,18 +97,9 @@ WorkspaceLayout workspace_layout(const pks_decode_args& a) {
   L.ld = (int64_t)a.max_pages * a.page_size;
   L.nchunks = (int)std::max<int64_t>(1, (L.ld + kTopkChunk - 1) / kTopkChunk);
 
-  int splits = a.attn_splits;
-  if (splits <= 0) {
-    const int64_t per = std::max<int64_t>(1, B * a.Hkv);
-    splits = (int)std::max<int64_t>(1, (kAttnTargetCtas + per - 1) / per);
-  }
-  const int max_splits = (a.k + kAttnTile - 1) / kAttnTile;
-  splits = std::min(std::max(splits, (a.k + kMaxSplitLen - 1) / kMaxSplitLen), max_splits);
-  splits = std::max(splits, 1);
-  int split_len = (a.k + splits - 1) / splits;
-  split_len = (split_len + kAttnTile - 1) / kAttnTile * kAttnTile;
-  L.split_len = split_len;
-  L.splits = (a.k + split_len - 1) / split_len;
+  L.attn_grid_max = kAttnGridMax;
+  const int hg = attn_heads_per_cta(a.Hkv);
+  const int64_t nseg = (int64_t)(a.Hkv / hg) * B;  // (head group, request) segments
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -124,14 +112,16 @@ WorkspaceLayout workspace_layout(const pks_decode_args& a) {
   L.hist = take(sizeof(int32_t) * (size_t)B * kScoreBins);
   L.tick_topk = take(sizeof(int32_t) * (size_t)B);
   L.cand_n = take(sizeof(int32_t) * (size_t)B);
-  L.tick_attn = take(sizeof(int32_t) * (size_t)B * a.Hkv);
   L.ctrl_end = off;
   L.scores = take(sizeof(int32_t) * (size_t)B * (size_t)L.ld);
   L.cand = take(sizeof(int32_t) * 2 * (size_t)B * (size_t)L.ld);
+  L.bits = take(sizeof(uint32_t) * (size_t)B * L.nchunks * (kTopkChunk / 32));
   L.gt_cnt = take(sizeof(int32_t) * (size_t)B * L.nchunks);
   L.chunk_off = take(sizeof(int32_t) * (size_t)B * L.nchunks);
   L.thresh = take(sizeof(TopkThreshold) * (size_t)B);
-  const size_t nslots = (size_t)B * a.Hkv * L.splits * G;
+  L.attn_prefix = take(sizeof(int32_t) * (size_t)(B + 1));
+  // partial (m, l, o) slots: one per (CTA, segment) pair, indexed cta + segment
+  const size_t nslots = (size_t)(L.attn_grid_max + nseg) * hg * G;
   L.part_ml = take(sizeof(float) * 2 * nslots);
   L.part_o = take(sizeof(float) * nslots * a.D);
   L.total = off;
@@ -337,7 +327,7 @@ static pks_status decode_impl(const pks_decode_args* args, pks_stream stream,
   if (e == cudaSuccess) e = rec(1);
   if (e == cudaSuccess) e = pks::launch_topk(*args, L, ws, s);
   if (e == cudaSuccess) e = rec(2);
-  if (e == cudaSuccess) e = pks::launch_attention(*args, L, ws, s);
+  if (e == cudaSuccess) e = pks::launch_attention(*args, L, ws, /*trim=*/true, s);
   if (e == cudaSuccess) e = rec(3);
   return pks::from_cuda(e);
 }
@@ -379,6 +369,7 @@ pks_status pks_sparse_attention(const pks_decode_args* args, pks_stream stream) 
   if ((st = pks::check_workspace(args, L)) != PKS_OK) return st;
   if (args->B == 0) return PKS_OK;
   return pks::from_cuda(pks::launch_attention(*args, L, static_cast<uint8_t*>(args->workspace),
+                                              /*trim=*/false,
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 

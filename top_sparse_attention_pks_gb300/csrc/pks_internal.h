@@ -17,14 +17,25 @@ namespace pks {
 constexpr int kScoreBins = 2048;
 // Tokens per top-k chunk (one CTA of the threshold and emit kernels).
 constexpr int kTopkChunk = 4096;
-// Attention: tokens per pipeline tile and positions per split granule.
-constexpr int kAttnTile = 64;
+// Attention: tokens per pipeline tile; largest persistent grid the workspace
+// holds partials for.
+constexpr int kAttnTile = 16;
+constexpr int kAttnGridMax = 1024;
+
+// KV heads handled by one attention CTA (one warp each): the largest of
+// 8, 4, 2, 1 that divides Hkv.
+inline int attn_heads_per_cta(int hkv) {
+  for (int hg = 8; hg > 1; hg >>= 1)
+    if (hkv % hg == 0) return hg;
+  return 1;
+}
 
 // Device error word causes (see pks_decode_device_error).
 constexpr int kErrPage = 1;
 constexpr int kErrToken = 2;
 constexpr int kErrLen = 3;
 constexpr int kErrState = 4;
+constexpr int kErrTimeout = 5;
 // header word 5 of a residency state filled by pks_residency_init
 constexpr int32_t kResidencyMagic = 0x504b5352;
 
@@ -38,13 +49,12 @@ struct TopkThreshold {
 // starts on a 256-byte boundary.  The control block (error word, histograms,
 // tickets, counters) must be zero between steps; everything else is scratch.
 struct WorkspaceLayout {
-  size_t ctrl, err, hist, tick_topk, cand_n, tick_attn, ctrl_end;
-  size_t scores, cand, gt_cnt, chunk_off, thresh, part_ml, part_o;
+  size_t ctrl, err, hist, tick_topk, cand_n, ctrl_end;
+  size_t scores, cand, bits, gt_cnt, chunk_off, thresh, attn_prefix, part_ml, part_o;
   size_t total;
   int64_t ld;          // score row stride (max_pages * page_size)
-  int32_t nchunks;     // top-k chunks per request
-  int32_t splits;      // attention splits per (request, kv head)
-  int32_t split_len;   // top-k positions per split (multiple of kAttnTile)
+  int32_t nchunks;       // top-k chunks per request
+  int32_t attn_grid_max; // attention CTAs the partial slots are sized for
 };
 
 WorkspaceLayout workspace_layout(const pks_decode_args& a);
@@ -54,8 +64,13 @@ cudaError_t launch_indexer_scan(const pks_decode_args& a, int32_t* scores, int64
                                 int32_t* hist, int32_t* err, cudaStream_t s);
 cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
                         cudaStream_t s);
+// kernels launch_topk enqueues for these shapes (1, or 2 for contexts longer
+// than the shared-memory bitmap)
+int topk_kernel_launches(const pks_decode_args& a);
+// trim: the top-k list holds its selected entries first (the step's own
+// output), so only min(k, len_b) positions per request are visited.
 cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
-                             cudaStream_t s);
+                             bool trim, cudaStream_t s);
 cudaError_t launch_residency(int32_t* state, int32_t num_pages, int32_t capacity, int32_t B,
                              int32_t k, int32_t page_size, int32_t max_pages,
                              const int32_t* topk_idx, const int32_t* block_table,
