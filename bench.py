@@ -291,10 +291,9 @@ def main():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         one_step(s)
-    # scan, top-k threshold (+ top-k emit beyond 131072-token contexts),
-    # attention + merge, (+ residency mark and update)
-    launches_per_step = (4 + (1 if wl.max_pages * wl.page_size > 131072 else 0)
-                         + (2 if res is not None else 0))
+    # scan, top-k, attention + merge as the library reports them (+ residency
+    # mark and update)
+    launches_per_step = step.launches() + (2 if res is not None else 0)
 
     with torch.cuda.stream(s):
         for _ in range(args.warmup):

@@ -146,7 +146,9 @@ typedef struct pks_decode_args {
   int32_t attn_splits;    /* attention CTAs: 0 = one per resident slot on the GPU; else this
                              many (1..1024), each taking an equal share of all selected
                              (KV head group, request, position) work */
-  int32_t reserved[3];    /* must be 0 */
+  int32_t topk_mode;      /* 0 = one cooperative top-k launch when its grid fits on the GPU
+                             at once, else two; 1 = always the two-kernel path */
+  int32_t reserved[2];    /* must be 0 */
 } pks_decode_args;
 
 /* Workspace bytes a step with these shapes needs (pointers may be NULL). */
@@ -157,9 +159,18 @@ pks_status pks_decode_workspace_size(const pks_decode_args* args, size_t* bytes)
  * leaves them zero again, so steps can be replayed (e.g. in a CUDA graph). */
 pks_status pks_decode_workspace_init(const pks_decode_args* args, pks_stream stream);
 
-/* The whole step: scan, top-k, attention.  Four kernel launches (five when
- * max_pages*page_size exceeds 131072 tokens). */
+/* The whole step: scan, top-k, attention.  Three or four kernel launches:
+ * scan, top-k, attention and merge; top-k is one cooperative launch when all
+ * of its (4096-token chunk, request) CTAs fit on the device at once, else two
+ * (three with more than 131072 tokens per request); see pks_decode_launches.
+ * TIMEOUT-class failures of the top-k barrier are reported through
+ * pks_decode_device_error (code 5), after which the workspace must be
+ * re-initialised. */
 pks_status pks_decode_step(const pks_decode_args* args, pks_stream stream);
+
+/* Kernels one pks_decode_step with these shapes enqueues on the current
+ * device (host only; pointers may be NULL).  INVALID: bad shapes or out NULL. */
+pks_status pks_decode_launches(const pks_decode_args* args, int32_t* launches);
 
 /* Same as pks_decode_step, recording events[0..3] (nullable entries) before the
  * scan, after the scan, after the top-k kernels and after attention. */

@@ -51,27 +51,39 @@ def oracle_topk(wl, t, requests=None):
 
 
 def oracle_attention(wl, t, idx, requests=None):
-    """Oracle attention for the given selection; copies only the pages the
-    requests use (remapped to a compact pool)."""
-    bt = host(t["block_table"]).numpy()
+    """Oracle attention for the given selection (all requests or a subset).
+
+    Only the K/V rows the selection reads leave the device: the host gathers
+    them into a compact pool of one-token pages (row j of request b's block
+    row is the j-th selected token), and the oracle runs on that pool with
+    page_size 1.  The physical row of each token is found on the host from
+    the real block table."""
+    bt = host(t["block_table"]).numpy().astype(np.int64)
     lens = host(t["seq_lens"]).numpy()
     q = host(t["q"])
+    idx = np.asarray(idx)
     if requests is not None:
-        bt, lens, q = bt[requests], lens[requests], q[requests]
+        requests = np.asarray(requests)
+        bt, lens, q, idx = bt[requests], lens[requests], q[requests], idx[requests]
     P = wl.page_size
-    used = []
-    for b in range(bt.shape[0]):
-        used.extend(bt[b, : -(-int(lens[b]) // P)].tolist())
-    pages = np.unique(np.asarray(used, dtype=np.int64))
-    remap = {int(p): i for i, p in enumerate(pages)}
-    bt_c = np.full_like(bt, -1)
-    for b in range(bt.shape[0]):
-        n = -(-int(lens[b]) // P)
-        bt_c[b, :n] = [remap[int(p)] for p in bt[b, :n]]
-    sel = torch.from_numpy(pages).to(t["kv_k"].device)
-    kk = host(t["kv_k"].index_select(0, sel))
-    vv = host(t["kv_v"].index_select(0, sel))
-    return oracle.sparse_attention(bt_c, P, idx, q, kk, vv)
+    B, k = idx.shape
+    max_len = int(max(1, idx.max() + 1)) if idx.size else 1
+    rows, bt_c = [], np.full((B, max_len), -1, np.int32)
+    for b in range(B):
+        sel = idx[b][idx[b] >= 0]
+        assert (sel < lens[b]).all(), "selection beyond the request's length"
+        phys = bt[b, sel // P] * P + sel % P
+        bt_c[b, sel] = np.arange(len(rows), len(rows) + len(sel), dtype=np.int32)
+        rows.extend(phys.tolist())
+    dev = t["kv_k"].device
+    Hkv, D = t["kv_k"].shape[2], t["kv_k"].shape[3]
+    r = torch.as_tensor(np.asarray(rows, dtype=np.int64), device=dev)
+    kk = host(t["kv_k"].reshape(-1, Hkv, D).index_select(0, r)).reshape(-1, 1, Hkv, D)
+    vv = host(t["kv_v"].reshape(-1, Hkv, D).index_select(0, r)).reshape(-1, 1, Hkv, D)
+    if len(rows) == 0:
+        kk = torch.zeros((1, 1, Hkv, D), dtype=torch.bfloat16)
+        vv = torch.zeros((1, 1, Hkv, D), dtype=torch.bfloat16)
+    return oracle.sparse_attention(bt_c, 1, idx, q, kk, vv)
 
 
 def check_attention(got: torch.Tensor, ref: np.ndarray, what=""):
@@ -86,8 +98,8 @@ def check_attention(got: torch.Tensor, ref: np.ndarray, what=""):
     return max_abs, rel
 
 
-def run_step(wl, t, attn_splits=0):
-    step = SparseDecodeStep(t, wl.k, attn_splits=attn_splits)
+def run_step(wl, t, attn_splits=0, topk_mode=0):
+    step = SparseDecodeStep(t, wl.k, attn_splits=attn_splits, topk_mode=topk_mode)
     out, idx = step()
     torch.cuda.synchronize()
     return step, out, idx

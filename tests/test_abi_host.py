@@ -166,7 +166,7 @@ def test_workspace_size_and_validation_without_gpu():
     # no workspace -> PKS_ERR_WORKSPACE, before any device work
     assert L.pks_decode_step(ctypes.byref(a), None) == -7
     cases = [dict(Hq=6, Hkv=4), dict(k=0), dict(page_size=0), dict(B=-1),
-             dict(reserved=(ctypes.c_int32 * 3)(1, 0, 0)), dict(attn_splits=-2),
+             dict(reserved=(ctypes.c_int32 * 2)(1, 0)), dict(topk_mode=2), dict(topk_mode=-1), dict(attn_splits=-2),
              dict(attn_splits=1025)]
     for c in cases:
         assert L.pks_decode_workspace_size(ctypes.byref(_cpu_args(**c)),

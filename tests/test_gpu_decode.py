@@ -22,8 +22,8 @@ def _built():
     build.build_library()
 
 
-def full_check(wl, t, attn_splits=0, check_scores=True):
-    step, out, idx = run_step(wl, t, attn_splits)
+def full_check(wl, t, attn_splits=0, check_scores=True, topk_mode=0):
+    step, out, idx = run_step(wl, t, attn_splits, topk_mode)
     ref_scores, ref_idx = oracle_topk(wl, t)
     if check_scores:
         sc = host(step.scores()).numpy().astype(np.int64)
@@ -38,10 +38,11 @@ def full_check(wl, t, attn_splits=0, check_scores=True):
     return step, out, got_idx
 
 
-def test_paging_example_config():
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_paging_example_config(topk_mode):
     wl = WORKLOADS["paging_example"]
     t, _, _ = prepare(wl)
-    full_check(wl, t)
+    full_check(wl, t, topk_mode=topk_mode)
 
 
 @pytest.mark.parametrize("over", [
@@ -60,12 +61,13 @@ def test_paging_example_variants(over):
     full_check(wl, t)
 
 
-def test_all_scores_tied():
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_all_scores_tied(topk_mode):
     # zero indexer queries: every score is 0, selection = lowest indices
     wl = WORKLOADS["paging_example"]
     t, _, _ = prepare(wl)
     t["q_idx"].zero_()
-    _, _, idx = full_check(wl, t)
+    _, _, idx = full_check(wl, t, topk_mode=topk_mode)
     for b, n in enumerate(wl.seq_lens):
         expect = list(range(min(n, wl.k))) + [-1] * max(0, wl.k - n)
         assert idx[b].tolist() == expect
@@ -88,40 +90,48 @@ def test_attention_split_counts(splits):
     full_check(wl, t, attn_splits=splits)
 
 
-def test_b32_4k_reduced():
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_b32_4k_reduced(topk_mode):
     wl = WORKLOADS["b32_4k"].replace(B=4, seq_lens=(4096,) * 4, num_pages=256)
     t, _, _ = prepare(wl)
-    full_check(wl, t)
+    full_check(wl, t, topk_mode=topk_mode)
 
 
-def test_ragged_prefix_reduced():
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_ragged_prefix_reduced(topk_mode):
     wl = WORKLOADS["b64_ragged_prefix"].replace(B=16, num_pages=16 * 2048)
     t, _, bt = prepare(wl)
     # aliased prefix pages are shared by the rows of a group
     assert (bt[1, :125] == bt[0, :125]).all() or host(t["seq_lens"])[1] < 2000
-    full_check(wl, t)
+    full_check(wl, t, topk_mode=topk_mode)
 
 
-def test_128k_reduced():
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_128k_reduced(topk_mode):
     wl = WORKLOADS["b16_128k"].replace(B=2, seq_lens=(131072, 131072), num_pages=4096)
     t, _, _ = prepare(wl)
-    full_check(wl, t)
+    full_check(wl, t, topk_mode=topk_mode)
 
 
-def test_long_request_emit_path():
-    # a context longer than the top-k bitmap (131072 tokens) goes through the
-    # chunked emit kernel; a second, short request keeps the bitmap path
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_long_request_emit_path(topk_mode):
+    # two-kernel path: a context longer than the top-k bitmap (131072 tokens)
+    # goes through the chunked emit kernel, a second, short request keeps the
+    # bitmap path; cooperative path: 35 chunks of one request meet at the barrier
     wl = WORKLOADS["paging_example"].replace(
         B=2, seq_lens=(140000, 5000), page_size=64, max_pages=2200, num_pages=2300, k=512,
         Di=64, D=64, Hq=8, Hkv=2)
     t, _, _ = prepare(wl)
-    full_check(wl, t)
+    step, _, _ = full_check(wl, t, topk_mode=topk_mode)
+    # scan + top-k (one cooperative launch, or threshold + emit) + attention + merge
+    assert step.launches() == (4 if topk_mode == 0 else 5)
 
 
-def test_graph_replay_matches_eager():
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_graph_replay_matches_eager(topk_mode):
     wl = WORKLOADS["paging_example"].replace(k=128)
     t, _, _ = prepare(wl)
-    step = SparseDecodeStep(t, wl.k)
+    step = SparseDecodeStep(t, wl.k, topk_mode=topk_mode)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):

@@ -415,19 +415,22 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   }
 }
 
-// Combine the partial (m, l, o) of a segment's contributing CTAs: one CTA per
-// (KV head, request); segments one attention CTA owned whole are skipped (it
-// wrote the output itself).  Step 1: per query row, the max and 1/sum over the
-// contributors (lanes split the contributors, warps split the rows).
-// Step 2: threads own float4 columns; contributors are read four at a time.
+// Combine the partial (m, l, o) of a segment's contributing CTAs: one warp per
+// (query head, request); segments that one attention CTA owned whole are
+// skipped (it wrote the output itself).  Lanes split the contributors to find
+// the row's max and sum, then each lane accumulates float4 columns of o with
+// eight contributors' loads in flight at a time.
 template <int D>
 __global__ void __launch_bounds__(128)
 k_attention_merge(const int32_t* __restrict__ prefix, const float2* __restrict__ part_ml,
                   const float* __restrict__ part_o, __nv_bfloat16* __restrict__ out, int B,
                   int Hq, int Hkv, int HG, int G, int attn_grid) {
-  __shared__ float s_m[16], s_il[16];
   const float kNegInf = __int_as_float(0xff800000);
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qh = blockIdx.x * 4 + (threadIdx.x >> 5);  // query head
+  const int b = blockIdx.y;
+  if (qh >= Hq) return;
+  const int h = qh / G, gg = qh % G;  // KV head and row within its group
   const int g = h / HG, hh = h % HG;
   const int64_t Treq = prefix[B];
   const int64_t T = Treq * (Hkv / HG);
@@ -439,66 +442,51 @@ k_attention_merge(const int32_t* __restrict__ prefix, const float2* __restrict__
   if (c_first == c_last) return;
   const int seg = g * B + b;
   const int64_t pstride = (int64_t)HG * G;
-  // partial of contributor c, row gg: index (c + seg) * pstride + hh * G + gg
-  auto pidx = [&](int c, int gg) { return ((int64_t)c + seg) * pstride + (int64_t)hh * G + gg; };
+  auto pidx = [&](int c) { return ((int64_t)c + seg) * pstride + (int64_t)hh * G + gg; };
 
-  for (int gg = warp; gg < G; gg += 4) {
-    float M = kNegInf;
-    for (int c = c_first + lane; c <= c_last; c += 32) M = fmaxf(M, __ldcg(&part_ml[pidx(c, gg)].x));
+  float M = kNegInf;
+  for (int c = c_first + lane; c <= c_last; c += 32) M = fmaxf(M, __ldcg(&part_ml[pidx(c)].x));
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    if (M != kNegInf)
-      for (int c = c_first + lane; c <= c_last; c += 32) {
-        const float2 ml = __ldcg(&part_ml[pidx(c, gg)]);
-        if (ml.x != kNegInf) L += ml.y * exp2f(ml.x - M);
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = 0.f;
+  if (M != kNegInf)
+    for (int c = c_first + lane; c <= c_last; c += 32) {
+      const float2 ml = __ldcg(&part_ml[pidx(c)]);
+      if (ml.x != kNegInf) L += ml.y * exp2f(ml.x - M);
+    }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float il = L > 0.f ? 1.f / L : 0.f;
+
+  constexpr int DV4 = D / 4;  // float4 columns of a row (32 or 16)
+  if (lane >= DV4) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = c_first; c0 <= c_last; c0 += 8) {
+    float m[8];
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u;
+      if (c <= c_last) {
+        m[u] = __ldcg(&part_ml[pidx(c)].x);
+        v[u] = __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c) * D) + lane);
+      } else {
+        m[u] = kNegInf;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) {
-      s_m[gg] = M;
-      s_il[gg] = L > 0.f ? 1.f / L : 0.f;
+    for (int u = 0; u < 8; ++u) {
+      const float f = m[u] == kNegInf ? 0.f : exp2f(m[u] - M);
+      acc.x += f * v[u].x;
+      acc.y += f * v[u].y;
+      acc.z += f * v[u].z;
+      acc.w += f * v[u].w;
     }
   }
-  __syncthreads();
-
-  constexpr int DV4 = D / 4;
-  for (int it = tid; it < G * DV4; it += 128) {
-    const int gg = it / DV4, c4 = it % DV4;
-    const float M = s_m[gg];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int c = c_first;
-    for (; c + 3 <= c_last; c += 4) {
-      float m[4];
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        m[u] = __ldcg(&part_ml[pidx(c + u, gg)].x);
-        v[u] = __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c + u, gg) * D) + c4);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float f = m[u] == kNegInf ? 0.f : exp2f(m[u] - M);
-        acc.x += f * v[u].x;
-        acc.y += f * v[u].y;
-        acc.z += f * v[u].z;
-        acc.w += f * v[u].w;
-      }
-    }
-    for (; c <= c_last; ++c) {
-      const float mu = __ldcg(&part_ml[pidx(c, gg)].x);
-      const float4 vu = __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c, gg) * D) + c4);
-      const float f = mu == kNegInf ? 0.f : exp2f(mu - M);
-      acc.x += f * vu.x;
-      acc.y += f * vu.y;
-      acc.z += f * vu.z;
-      acc.w += f * vu.w;
-    }
-    const float il = s_il[gg];
-    __nv_bfloat16* dst = out + ((int64_t)b * Hq + (int64_t)h * G + gg) * D + c4 * 4;
-    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * il, acc.y * il);
-    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * il, acc.w * il);
-  }
+  __nv_bfloat16* dst = out + ((int64_t)b * Hq + qh) * D + lane * 4;
+  *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * il, acc.y * il);
+  *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * il, acc.w * il);
 }
 
 template <int D, int HG>
@@ -541,7 +529,7 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
       a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, trim ? 1 : 0, scale_log2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_attention_merge<D><<<dim3(a.Hkv, a.B), 128, 0, s>>>(
+  k_attention_merge<D><<<dim3((a.Hq + 3) / 4, a.B), 128, 0, s>>>(
       reinterpret_cast<const int32_t*>(ws + L.attn_prefix),
       reinterpret_cast<const float2*>(ws + L.part_ml), reinterpret_cast<const float*>(ws + L.part_o),
       reinterpret_cast<__nv_bfloat16*>(a.out), a.B, a.Hq, a.Hkv, HG, G, grid);

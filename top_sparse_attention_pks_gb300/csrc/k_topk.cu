@@ -7,22 +7,27 @@
 // is unique: the k largest of the composite key (score, -index).
 //
 // No sort.  The indexer scan leaves a 2048-bin histogram of each request's
-// scores (bins ordered like the scores).  k_topk_threshold runs one CTA per
-// (4096-token chunk, request):
-//  * every CTA finds the threshold bin T1 (the bin holding the k-th largest
-//    score), writes the bits of its tokens above T1 into the request's token
-//    bitmap (one warp ballot = one 32-token word, no atomics) and appends its
-//    tokens in T1 to the candidate list (one atomic per CTA);
-//  * the last CTA of a request to finish (atomic ticket, no CTA ever waits)
-//    radix-selects, 8 bits at a time and starting after the bits all
-//    candidates share, the exact threshold key among the candidates (a few
-//    hundred in practice) and adds the selected candidates to the bitmap.
-//    For requests up to 131072 tokens it then copies the bitmap to shared
-//    memory and writes the k selected indices in ascending order with one
-//    block scan; for longer requests it computes per-chunk offsets and
-//    k_topk_emit writes each chunk's indices from its 128 bitmap words.
-//    It leaves the histogram and counters zero for the next step.
-// Dense requests (len <= k) are written directly.
+// scores (bins ordered like the scores).  One CTA per (4096-token chunk,
+// request) runs the chunk phase: it finds the threshold bin T1 (the bin
+// holding the k-th largest score), counts its tokens above T1 and appends its
+// tokens in T1 to the request's candidate list (one atomic per CTA).  The
+// exact threshold key among the candidates (a few hundred in practice) is
+// then radix-selected 8 bits at a time, starting after the bits all
+// candidates share.
+//
+// k_topk_select (one cooperative launch, used whenever the grid fits on the
+// GPU at once): the CTAs of a request meet at a counter barrier after the
+// chunk phase; each then selects the threshold itself and writes its own
+// chunk's indices at the chunk's output offset, so no CTA runs a serial tail.
+//
+// k_topk_threshold (+ k_topk_emit), the fallback for larger grids: no CTA
+// waits; the last CTA of a request to finish (atomic ticket) selects the
+// threshold, merges the selected candidates into the request's token bitmap
+// and writes the indices, or, beyond 131072 tokens, per-chunk offsets that
+// k_topk_emit turns into indices.
+//
+// Dense requests (len <= k) are written directly.  Both paths leave the
+// histogram and counters zero for the next step.
 
 #include "pks_internal.h"
 
@@ -35,6 +40,8 @@ constexpr int kPerThread = kTopkChunk / kTopkThreads;
 constexpr int kCandCap = 2048;
 // requests up to this many tokens are emitted through the shared bitmap
 constexpr int kBitmapTokens = 131072;
+// polls of a request barrier before it gives up (about 0.4 s)
+constexpr int kBarrierSpins = 1 << 22;
 
 __device__ __forceinline__ int score_bin(int s) {
   if (s == 0) return kScoreBins / 2;
@@ -96,7 +103,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_wa
 
 struct TopkWs {
   int32_t* hist;       // [B][kScoreBins]   control
-  int32_t* tick;       // [B]               control
+  int32_t* tick;       // [B]               control: ticket / barrier arrivals
+  int32_t* depart;     // [B]               control: barrier departures
   int32_t* cand_n;     // [B]               control
   int2* cand;          // [B][max_len]      (score, token) of bin-T1 tokens
   uint32_t* bits;      // [B][nchunks*128]  selected-token bitmap, 32 tokens a word
@@ -106,51 +114,35 @@ struct TopkWs {
   int32_t* err;
 };
 
-__global__ void __launch_bounds__(kTopkThreads)
-k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ scores,
-                 int64_t ld, TopkWs w, int32_t* __restrict__ topk, int k, int max_len,
-                 int nchunks_max) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  // [kCandCap] staged candidate keys | [kBitmapTokens/32] bitmap | [nchunks] counts
-  uint64_t* s_key = reinterpret_cast<uint64_t*>(dsm);
-  uint32_t* s_bm = reinterpret_cast<uint32_t*>(dsm + sizeof(uint64_t) * kCandCap);
-  int* s_cnt = reinterpret_cast<int*>(dsm + sizeof(uint64_t) * kCandCap + kBitmapTokens / 8);
-  __shared__ int s_warp[kTopkThreads / 32];
-  __shared__ int s_bins[kTopkThreads];
-  __shared__ int s_T1, s_above, s_last;
-  __shared__ int s_digit, s_digit_above, s_digit_count;
-  __shared__ unsigned long long s_and[kTopkThreads / 32], s_or[kTopkThreads / 32];
+// Shared memory of the chunk phase and the exact select.
+struct TopkSmem {
+  int warp[kTopkThreads / 32];
+  int bins[kTopkThreads];
+  int T1, above, flag;
+  int digit, digit_above, digit_count;
+  int cand_base;
+  unsigned long long kand[kTopkThreads / 32], kor[kTopkThreads / 32];
+};
 
-  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  const int len = clamp_len(seq_lens[b], max_len);
-  int32_t* row = topk + (int64_t)b * k;
-
-  if (len <= k) {
-    // dense: every token, then -1 padding
-    const int nch = max(1, (len + kTopkChunk - 1) / kTopkChunk);
-    if (c >= nch) return;
-    const int start = c * kTopkChunk, stop = min(len, start + kTopkChunk);
-    for (int t = start + tid; t < stop; t += kTopkThreads) row[t] = t;
-    if (c == 0)
-      for (int j = len + tid; j < k; j += kTopkThreads) row[j] = -1;
-    return;
-  }
-  const int nch = (len + kTopkChunk - 1) / kTopkChunk;
-  if (c >= nch) return;
-
-  // ---- chunk scores first (independent of the histogram): one L2 latency
-  const int start = c * kTopkChunk, stop = min(len, start + kTopkChunk);
-  const int32_t* sb = scores + (int64_t)b * ld;
-  int sc[kPerThread];
+// Chunk phase, run by every CTA of a request: load the chunk's scores, find
+// the threshold bin T1 from the request's histogram, count the chunk's tokens
+// above T1 and append its bin-T1 tokens to the candidate list.  Returns false
+// (and flags kErrState once) when the histogram counts fewer than k tokens.
+// With `bitmap` it also writes the chunk's above-T1 bitmap words.
+__device__ __forceinline__ bool chunk_phase(const int32_t* __restrict__ sb, const int32_t* hb,
+                                            int start, int stop, int k, int2* cb, int cand_cap,
+                                            int32_t* cand_n,
+                                            uint32_t* bw, bool bitmap, int32_t* err, bool report,
+                                            int (&sc)[kPerThread], int& T1, int& above,
+                                            int& gt_total, TopkSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // chunk scores first (independent of the histogram): one L2 latency
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     const int t = start + j * kTopkThreads + tid;
     sc[j] = t < stop ? sb[t] : 0;
   }
-
-  // ---- threshold bin: the bin where the count from the top reaches k
-  const int32_t* hb = w.hist + (int64_t)b * kScoreBins;
+  // threshold bin: the bin where the count from the top reaches k
   constexpr int kPer = kScoreBins / kTopkThreads;
   int h[kPer];
   int local = 0;
@@ -160,38 +152,35 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
     local += h[i];
   }
   if (tid == 0) {
-    s_T1 = -1;
-    s_above = 0;
+    sm.T1 = -1;
+    sm.above = 0;
   }
-  s_bins[kTopkThreads - 1 - tid] = local;  // suffix sums = scan in reversed order
+  sm.bins[kTopkThreads - 1 - tid] = local;  // suffix sums = scan in reversed order
   __syncthreads();
   int total;
-  const int rev_before = block_exclusive_scan<kTopkThreads>(s_bins[tid], &total, s_warp);
+  const int rev_before = block_exclusive_scan<kTopkThreads>(sm.bins[tid], &total, sm.warp);
   __syncthreads();
-  s_bins[kTopkThreads - 1 - tid] = rev_before;  // tokens in bins above this thread's bins
+  sm.bins[kTopkThreads - 1 - tid] = rev_before;  // tokens in bins above this thread's bins
   __syncthreads();
   {
-    int run = s_bins[tid];
+    int run = sm.bins[tid];
 #pragma unroll
     for (int i = kPer - 1; i >= 0; --i) {
       if (run < k && run + h[i] >= k) {
-        s_T1 = tid * kPer + i;
-        s_above = run;
+        sm.T1 = tid * kPer + i;
+        sm.above = run;
       }
       run += h[i];
     }
   }
   __syncthreads();
-  const int T1 = s_T1;
+  T1 = sm.T1;
+  above = sm.above;
   if (T1 < 0) {
     // fewer than k tokens counted: the workspace was not initialised
-    if (tid == 0 && c == 0) atomicCAS(w.err, 0, kErrState);
-    return;
+    if (tid == 0 && report) atomicCAS(err, 0, kErrState);
+    return false;
   }
-
-  // ---- tokens above T1 (bitmap words) and candidates (tokens in T1)
-  int2* cb = w.cand + (int64_t)b * max_len;
-  uint32_t* bw = w.bits + (int64_t)b * nchunks_max * (kTopkChunk / 32);
   int gt = 0, n_eq = 0;
   unsigned eqm = 0;  // bit j: this thread's token of slice j is a candidate
 #pragma unroll
@@ -202,7 +191,7 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
     // slice j of warp `warp` is the aligned 32-token word at t - lane
     const unsigned m = __ballot_sync(0xffffffffu, valid && bin > T1);
     if (lane == 0) {
-      bw[(start + j * kTopkThreads + warp * 32) >> 5] = m;
+      if (bitmap) bw[(start + j * kTopkThreads + warp * 32) >> 5] = m;
       gt += __popc(m);
     }
     if (valid && bin == T1) {
@@ -212,19 +201,541 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
   }
   // one atomic per CTA reserves the candidates' slots
   int n_eq_total;
-  int eq_base = block_exclusive_scan<kTopkThreads>(n_eq, &n_eq_total, s_warp);
-  __shared__ int s_cand_base;
-  if (tid == 0) s_cand_base = n_eq_total ? atomicAdd(w.cand_n + b, n_eq_total) : 0;
+  int eq_base = block_exclusive_scan<kTopkThreads>(n_eq, &n_eq_total, sm.warp);
+  if (tid == 0) sm.cand_base = n_eq_total ? atomicAdd(cand_n, n_eq_total) : 0;
   __syncthreads();
-  eq_base += s_cand_base;
+  eq_base += sm.cand_base;
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     if (eqm & (1u << j)) {
-      if (eq_base < max_len) cb[eq_base] = make_int2(sc[j], start + j * kTopkThreads + tid);
+      if (eq_base < cand_cap) cb[eq_base] = make_int2(sc[j], start + j * kTopkThreads + tid);
       ++eq_base;
     }
   }
-  const int gt_total = block_sum<kTopkThreads>(gt, s_warp);
+  gt_total = block_sum<kTopkThreads>(gt, sm.warp);
+  return true;
+}
+
+// Exact threshold key among the n candidates: the need-th largest
+// (score, ~token) key, radix-selected 8 bits at a time after the leading bits
+// that every candidate shares.  Candidates are staged in s_key when they fit,
+// else re-read from the list in L2 on every pass.  Block-wide; every thread
+// returns the key.
+__device__ __forceinline__ uint64_t exact_threshold(const int2* cb, int n, int need,
+                                                    uint64_t* s_key, TopkSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool staged = n <= kCandCap;
+  uint64_t kand = ~0ull, kor = 0ull;
+  for (int i = tid; i < n; i += kTopkThreads) {
+    const int2 e = __ldcg(cb + i);
+    const uint64_t key = order_key(e.x, e.y);
+    if (staged) s_key[i] = key;
+    kand &= key;
+    kor |= key;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    kand &= __shfl_xor_sync(0xffffffffu, kand, o);
+    kor |= __shfl_xor_sync(0xffffffffu, kor, o);
+  }
+  if (lane == 0) {
+    sm.kand[warp] = kand;
+    sm.kor[warp] = kor;
+  }
+  __syncthreads();
+  kand = ~0ull;
+  kor = 0ull;
+#pragma unroll
+  for (int i = 0; i < kTopkThreads / 32; ++i) {
+    kand &= sm.kand[i];
+    kor |= sm.kor[i];
+  }
+  const int common = n > 0 ? __clzll((long long)(kand ^ kor)) : 64;  // 64 when all equal
+  int bits = (common / 8) * 8;
+  uint64_t prefix = bits == 0 ? 0ull : (bits == 64 ? kand : (kand >> (64 - bits)));
+  while (bits < 64) {
+    const int shift = 56 - bits;
+    sm.bins[tid] = 0;
+    if (tid == 0) {
+      sm.digit = 0;
+      sm.digit_above = 0;
+      sm.digit_count = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kTopkThreads) {
+      uint64_t key;
+      if (staged) {
+        key = s_key[i];
+      } else {
+        const int2 e = __ldcg(cb + i);
+        key = order_key(e.x, e.y);
+      }
+      if (bits == 0 || (key >> (64 - bits)) == prefix)
+        atomicAdd(&sm.bins[(int)((key >> shift) & 255u)], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane owns digits [8*lane, 8*lane+8); find the digit where the count
+      // from the top reaches `need`
+      int d[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        d[i] = sm.bins[lane * 8 + i];
+        sum += d[i];
+      }
+      int incl = sum;  // suffix sum over lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      int run = incl - sum;
+#pragma unroll
+      for (int i = 7; i >= 0; --i) {
+        if (run < need && run + d[i] >= need) {
+          sm.digit = lane * 8 + i;
+          sm.digit_above = run;
+          sm.digit_count = d[i];
+        }
+        run += d[i];
+      }
+    }
+    __syncthreads();
+    need -= sm.digit_above;
+    prefix = (prefix << 8) | (uint64_t)sm.digit;
+    bits += 8;
+    const bool done = sm.digit_count == need;
+    __syncthreads();
+    if (done) break;
+  }
+  return bits == 64 ? prefix : (prefix << (64 - bits));
+}
+
+// Bounded wait until `count` CTAs of a request have arrived.  Called by one
+// thread after the CTA's writes are ordered by __syncthreads.
+__device__ __forceinline__ bool request_barrier(int32_t* arrive, int count) {
+  __threadfence();
+  atomicAdd(arrive, 1);
+  for (int it = 0; it < kBarrierSpins; ++it) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(arrive) : "memory");
+    if (v >= count) {
+      __threadfence();
+      return true;
+    }
+    if (it >= 32) __nanosleep(64);
+  }
+  return false;
+}
+
+// Dense request (len <= k): every token, then -1 padding.
+__device__ __forceinline__ void write_dense(int32_t* row, int len, int k, int c) {
+  const int start = c * kTopkChunk, stop = min(len, start + kTopkChunk);
+  for (int t = start + threadIdx.x; t < stop; t += kTopkThreads) row[t] = t;
+  if (c == 0)
+    for (int j = len + threadIdx.x; j < k; j += kTopkThreads) row[j] = -1;
+}
+
+// Single-launch selection for grids that fit on the GPU at once (launched
+// cooperatively, so all CTAs of a request are resident together).  One CTA
+// per (4096-token chunk, request); thread i owns the 4 consecutive tokens
+// 4i..4i+3 of each of the chunk's 4 rounds of 1024 tokens, read with one
+// 16-byte load per round (score rows are padded to whole chunks).
+//  1. Chunk phase: threshold bin T1 from the histogram; per-thread masks of
+//     the tokens above T1 and in T1; the chunk's T1 tokens go to the chunk's
+//     own region of the candidate buffer and its two counts to chunk_cnt
+//     (no atomics).
+//  2. Counter barrier of the request's CTAs.
+//  3. Every CTA gathers all candidates of the request (chunk order), selects
+//     the same exact threshold key, and writes its own chunk's selected
+//     tokens in ascending order at the chunk's output offset: tokens above T1
+//     in earlier chunks plus selected candidates of earlier chunks.
+// CTA 0 clears the histogram once every CTA has read it; the last CTA to
+// leave resets the request's barrier counters.
+constexpr int kVec = 4;                                          // tokens per load
+constexpr int kRounds = kTopkChunk / (kTopkThreads * kVec);      // 4
+constexpr int kSlices = kRounds * (kTopkThreads / 32);           // 32 (round, warp) slices
+
+template <typename KeyAt>
+__device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_at,
+                                                     TopkSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t kand = ~0ull, kor = 0ull;
+  for (int i = tid; i < n; i += kTopkThreads) {
+    const uint64_t key = key_at(i);
+    kand &= key;
+    kor |= key;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    kand &= __shfl_xor_sync(0xffffffffu, kand, o);
+    kor |= __shfl_xor_sync(0xffffffffu, kor, o);
+  }
+  if (lane == 0) {
+    sm.kand[warp] = kand;
+    sm.kor[warp] = kor;
+  }
+  __syncthreads();
+  kand = ~0ull;
+  kor = 0ull;
+#pragma unroll
+  for (int i = 0; i < kTopkThreads / 32; ++i) {
+    kand &= sm.kand[i];
+    kor |= sm.kor[i];
+  }
+  const int common = n > 0 ? __clzll((long long)(kand ^ kor)) : 64;  // 64 when all equal
+  int bits = (common / 8) * 8;
+  uint64_t prefix = bits == 0 ? 0ull : (bits == 64 ? kand : (kand >> (64 - bits)));
+  while (bits < 64) {
+    const int shift = 56 - bits;
+    sm.bins[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint64_t key = key_at(i);
+      if (bits == 0 || (key >> (64 - bits)) == prefix)
+        atomicAdd(&sm.bins[(int)((key >> shift) & 255u)], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane owns digits [8*lane, 8*lane+8); find the digit where the count
+      // from the top reaches `need`
+      int d[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        d[i] = sm.bins[lane * 8 + i];
+        sum += d[i];
+      }
+      int incl = sum;  // suffix sum over lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      int run = incl - sum;
+      int digit = 0, above = 0, count = 0;
+      bool hit = false;
+#pragma unroll
+      for (int i = 7; i >= 0; --i) {
+        if (run < need && run + d[i] >= need) {
+          digit = lane * 8 + i;
+          above = run;
+          count = d[i];
+          hit = true;
+        }
+        run += d[i];
+      }
+      const unsigned who = __ballot_sync(0xffffffffu, hit);
+      if (who == 0u) {
+        if (lane == 0) {  // inconsistent counts: settle on the lowest digit
+          sm.digit = 0;
+          sm.digit_above = 0;
+          sm.digit_count = 0;
+        }
+      } else if (lane == __ffs(who) - 1) {
+        sm.digit = digit;
+        sm.digit_above = above;
+        sm.digit_count = count;
+      }
+    }
+    __syncthreads();
+    need -= sm.digit_above;
+    prefix = (prefix << 8) | (uint64_t)sm.digit;
+    bits += 8;
+    const bool done = sm.digit_count == need;
+    __syncthreads();
+    if (done) break;
+  }
+  return bits == 64 ? prefix : (prefix << (64 - bits));
+}
+
+// four CTAs an SM (64 registers): 608 resident CTAs on 152 SMs
+__global__ void __launch_bounds__(kTopkThreads, 4)
+k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ scores,
+              int64_t ld, TopkWs w, int2* __restrict__ chunk_cnt, int32_t* __restrict__ topk,
+              int k, int max_len, int nchunks_max) {
+  __shared__ uint64_t s_key[kCandCap];
+  __shared__ int s_eqoff[kTopkCoopMaxChunks + 1];  // candidates before each chunk
+  __shared__ int s_slice[kSlices];
+  __shared__ int s_before;
+  __shared__ TopkSmem sm;
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int start = c * kTopkChunk;
+
+  // all loads of the chunk phase at once: scores (rows padded to whole
+  // chunks, so always in bounds), the histogram and the length
+  int4 v[kRounds];
+  {
+    const int4* sp = reinterpret_cast<const int4*>(scores + (int64_t)b * ld + start);
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) v[r] = __ldcg(sp + r * kTopkThreads + tid);
+  }
+  int32_t* hb = w.hist + (int64_t)b * kScoreBins;
+  constexpr int kPer = kScoreBins / kTopkThreads;  // 8 bins a thread
+  int h[kPer];
+  {
+    const int4 h0 = __ldcg(reinterpret_cast<const int4*>(hb) + 2 * tid);
+    const int4 h1 = __ldcg(reinterpret_cast<const int4*>(hb) + 2 * tid + 1);
+    h[0] = h0.x; h[1] = h0.y; h[2] = h0.z; h[3] = h0.w;
+    h[4] = h1.x; h[5] = h1.y; h[6] = h1.z; h[7] = h1.w;
+  }
+  const int len = clamp_len(seq_lens[b], max_len);
+  int32_t* row = topk + (int64_t)b * k;
+  if (len <= k) {
+    const int nch = max(1, (len + kTopkChunk - 1) / kTopkChunk);
+    if (c < nch) write_dense(row, len, k, c);
+    return;
+  }
+  const int nch = (len + kTopkChunk - 1) / kTopkChunk;
+  if (c >= nch) return;
+  const int stop = min(len, start + kTopkChunk);
+
+  // ---- threshold bin: the bin where the count from the top reaches k
+  int local = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) local += h[i];
+  if (tid == 0) sm.T1 = -1;
+  sm.bins[kTopkThreads - 1 - tid] = local;  // suffix sums = scan in reversed order
+  __syncthreads();
+  int total;
+  const int rev_before = block_exclusive_scan<kTopkThreads>(sm.bins[tid], &total, sm.warp);
+  __syncthreads();
+  sm.bins[kTopkThreads - 1 - tid] = rev_before;  // tokens in bins above this thread's bins
+  __syncthreads();
+  {
+    int run = sm.bins[tid];
+#pragma unroll
+    for (int i = kPer - 1; i >= 0; --i) {
+      if (run < k && run + h[i] >= k) {
+        sm.T1 = tid * kPer + i;
+        sm.above = run;
+      }
+      run += h[i];
+    }
+  }
+  __syncthreads();
+  const int T1 = sm.T1, above = sm.above;
+  if (T1 < 0) {
+    // fewer than k tokens counted: the workspace was not initialised (every
+    // CTA of the request reads the same histogram, so all return here)
+    if (tid == 0 && c == 0) atomicCAS(w.err, 0, kErrState);
+    return;
+  }
+
+  // ---- masks of this thread's tokens above T1 (gtm) and in T1 (eqm);
+  // bit r*4+e is token start + r*1024 + 4*tid + e
+  unsigned gtm = 0, eqm = 0;
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int sv[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      const int t = start + r * (kTopkThreads * kVec) + tid * kVec + e;
+      const int bin = score_bin(sv[e]);
+      const bool valid = t < stop;
+      gtm |= (unsigned)(valid && bin > T1) << (r * kVec + e);
+      eqm |= (unsigned)(valid && bin == T1) << (r * kVec + e);
+    }
+  }
+  // one scan of both counts: above-T1 in the high half, candidates in the low
+  int packed_total;
+  const int packed_before = block_exclusive_scan<kTopkThreads>(
+      (__popc(gtm) << 16) | __popc(eqm), &packed_total, sm.warp);
+  int2* cregion = w.cand + ((int64_t)b * nchunks_max + c) * kTopkChunk;
+  const int eq_before = packed_before & 0xffff;
+  if (eqm) {
+    int pos = eq_before;
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int sv[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+      for (int e = 0; e < kVec; ++e)
+        if ((eqm >> (r * kVec + e)) & 1u)
+          cregion[pos++] = make_int2(sv[e], start + r * (kTopkThreads * kVec) + tid * kVec + e);
+    }
+  }
+  if (tid == 0)
+    chunk_cnt[(int64_t)b * nchunks_max + c] = make_int2(packed_total >> 16, packed_total & 0xffff);
+
+  // ---- barrier of the request's CTAs
+  __syncthreads();
+  if (tid == 0) sm.flag = request_barrier(w.tick + b, nch);
+  __syncthreads();
+  if (!sm.flag) {
+    if (tid == 0) atomicCAS(w.err, 0, kErrTimeout);
+    return;
+  }
+  // every CTA has read the histogram: clear it for the next step
+  if (c == 0)
+    for (int i = tid; i < kScoreBins; i += kTopkThreads) hb[i] = 0;
+
+  // ---- per-chunk counts -> candidate offsets and this chunk's above-T1 offset
+  {
+    // nch <= kTopkCoopMaxChunks = 4 * kTopkThreads: up to 4 chunks a thread,
+    // their candidate counts parked in s_eqoff across the scan
+    const int per = (nch + kTopkThreads - 1) / kTopkThreads;
+    int eq_sum = 0, gt_before = 0;
+    for (int i = 0; i < per; ++i) {
+      const int cc = tid * per + i;
+      if (cc < nch) {
+        const int2 cnt = __ldcg(chunk_cnt + (int64_t)b * nchunks_max + cc);
+        s_eqoff[cc] = cnt.y;
+        eq_sum += cnt.y;
+        if (cc < c) gt_before += cnt.x;
+      }
+    }
+    int n_total;
+    int off = block_exclusive_scan<kTopkThreads>(eq_sum, &n_total, sm.warp);
+    for (int i = 0; i < per; ++i) {
+      const int cc = tid * per + i;
+      if (cc < nch) {
+        const int cnt = s_eqoff[cc];
+        s_eqoff[cc] = off;
+        off += cnt;
+      }
+    }
+    if (tid == 0) s_eqoff[nch] = n_total;
+    gt_before = block_sum<kTopkThreads>(gt_before, sm.warp);
+    if (tid == 0) s_before = gt_before;
+    __syncthreads();
+  }
+  const int n = s_eqoff[nch];
+  const int2* cbase = w.cand + (int64_t)b * nchunks_max * kTopkChunk;
+  // candidate i of the request, in chunk order
+  auto cand_at = [&](int i) -> int2 {
+    int lo = 0, hi = nch - 1;  // last chunk with s_eqoff <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_eqoff[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return __ldcg(cbase + (int64_t)lo * kTopkChunk + (i - s_eqoff[lo]));
+  };
+  const bool staged = n <= kCandCap;
+  if (staged) {
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const int2 e = cand_at(i);
+      s_key[i] = order_key(e.x, e.y);
+    }
+    __syncthreads();
+  }
+  auto key_at = [&](int i) -> uint64_t {
+    if (staged) return s_key[i];
+    const int2 e = cand_at(i);
+    return order_key(e.x, e.y);
+  };
+  const uint64_t kstar = select_threshold(n, k - above, key_at, sm);
+
+  // ---- output offset: above-T1 tokens and selected candidates of earlier chunks
+  int before = 0;
+  for (int i = tid; i < s_eqoff[c]; i += kTopkThreads) before += key_at(i) >= kstar;
+  before = s_before + block_sum<kTopkThreads>(before, sm.warp);
+
+  // ---- this chunk's selected tokens, ascending: round, warp, lane, element
+  // this thread's candidates sit in the request's list in token order from
+  // its chunk's offset plus its scan position
+  unsigned selm = gtm;
+  if (eqm) {
+    int i = s_eqoff[c] + eq_before;
+#pragma unroll
+    for (int bit = 0; bit < kRounds * kVec; ++bit)
+      if ((eqm >> bit) & 1u) {
+        if (key_at(i) >= kstar) selm |= 1u << bit;
+        ++i;
+      }
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  int lane_before[kRounds];  // selected tokens of lower lanes in this (round, warp) slice
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int mine = __popc((selm >> (r * kVec)) & 0xfu);
+    int x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    lane_before[r] = x - mine;
+    if (lane == 31) s_slice[r * (kTopkThreads / 32) + warp] = x;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int v0 = s_slice[lane];  // kSlices == 32: one slice a lane
+    int x = v0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    s_slice[lane] = x - v0;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    int pos = before + s_slice[r * (kTopkThreads / 32) + warp] + lane_before[r];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      if ((selm >> (r * kVec + e)) & 1u) {
+        if (pos < k) row[pos] = start + r * (kTopkThreads * kVec) + tid * kVec + e;
+        ++pos;
+      }
+    }
+  }
+
+  // the last CTA to leave resets the request's barrier counters
+  __syncthreads();
+  if (tid == 0) {
+    if (c == 0) {
+      TopkThreshold t;
+      t.bin = T1;
+      t.pad = 0;
+      t.key = kstar;
+      w.thr[b] = t;
+    }
+    __threadfence();
+    if (atomicAdd(w.depart + b, 1) == nch - 1) {
+      w.tick[b] = 0;
+      w.depart[b] = 0;
+    }
+  }
+}
+
+// Two-launch fallback for grids too large to be resident at once.  One CTA
+// per (chunk, request) runs the chunk phase and writes above-T1 bitmap words;
+// the last CTA of a request to finish (atomic ticket, no CTA ever waits)
+// selects the exact threshold, adds the selected candidates to the bitmap and
+// either emits the k indices itself through a shared-memory copy of the
+// bitmap (requests up to 131072 tokens) or computes per-chunk offsets for
+// k_topk_emit.
+__global__ void __launch_bounds__(kTopkThreads)
+k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ scores,
+                 int64_t ld, TopkWs w, int32_t* __restrict__ topk, int k, int max_len,
+                 int nchunks_max) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  // [kCandCap] staged candidate keys | [kBitmapTokens/32] bitmap | [nchunks] counts
+  uint64_t* s_key = reinterpret_cast<uint64_t*>(dsm);
+  uint32_t* s_bm = reinterpret_cast<uint32_t*>(dsm + sizeof(uint64_t) * kCandCap);
+  int* s_cnt = reinterpret_cast<int*>(dsm + sizeof(uint64_t) * kCandCap + kBitmapTokens / 8);
+  __shared__ TopkSmem sm;
+  __shared__ int s_last;
+
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int len = clamp_len(seq_lens[b], max_len);
+  int32_t* row = topk + (int64_t)b * k;
+  if (len <= k) {
+    const int nch = max(1, (len + kTopkChunk - 1) / kTopkChunk);
+    if (c < nch) write_dense(row, len, k, c);
+    return;
+  }
+  const int nch = (len + kTopkChunk - 1) / kTopkChunk;
+  if (c >= nch) return;
+  const int start = c * kTopkChunk, stop = min(len, start + kTopkChunk);
+  int2* cb = w.cand + (int64_t)b * max_len;
+  uint32_t* bw = w.bits + (int64_t)b * nchunks_max * (kTopkChunk / 32);
+  int sc[kPerThread];
+  int T1, above, gt_total;
+  if (!chunk_phase(scores + (int64_t)b * ld, w.hist + (int64_t)b * kScoreBins, start, stop, k,
+                   cb, max_len, w.cand_n + b, bw, true, w.err, c == 0, sc, T1, above, gt_total, sm))
+    return;
   if (tid == 0) w.gt_cnt[(int64_t)b * nchunks_max + c] = gt_total;
 
   // ---- ticket: the last chunk CTA of this request finishes the selection
@@ -238,93 +749,8 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
   __threadfence();
 
   const int n = min(__ldcg(w.cand_n + b), max_len);
-  int need = k - s_above;  // 1 <= need <= n when the workspace is consistent
   const bool staged = n <= kCandCap;
-  uint64_t kand = ~0ull, kor = 0ull;
-  for (int i = tid; i < n; i += kTopkThreads) {
-    const int2 e = __ldcg(cb + i);
-    const uint64_t key = order_key(e.x, e.y);
-    if (staged) s_key[i] = key;
-    kand &= key;
-    kor |= key;
-  }
-  // leading bits shared by every candidate need no pass
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    kand &= __shfl_xor_sync(0xffffffffu, kand, o);
-    kor |= __shfl_xor_sync(0xffffffffu, kor, o);
-  }
-  if (lane == 0) {
-    s_and[warp] = kand;
-    s_or[warp] = kor;
-  }
-  __syncthreads();
-  kand = ~0ull;
-  kor = 0ull;
-#pragma unroll
-  for (int i = 0; i < kTopkThreads / 32; ++i) {
-    kand &= s_and[i];
-    kor |= s_or[i];
-  }
-  const int common = n > 0 ? __clzll((long long)(kand ^ kor)) : 64;  // 64 when all equal
-  int bits = (common / 8) * 8;
-  uint64_t prefix = bits == 0 ? 0ull : (bits == 64 ? kand : (kand >> (64 - bits)));
-  while (bits < 64) {
-    const int shift = 56 - bits;
-    s_bins[tid] = 0;
-    if (tid == 0) {
-      s_digit = 0;
-      s_digit_above = 0;
-      s_digit_count = 0;
-    }
-    __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) {
-      uint64_t key;
-      if (staged) {
-        key = s_key[i];
-      } else {
-        const int2 e = __ldcg(cb + i);
-        key = order_key(e.x, e.y);
-      }
-      if (bits == 0 || (key >> (64 - bits)) == prefix)
-        atomicAdd(&s_bins[(int)((key >> shift) & 255u)], 1);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane owns digits [8*lane, 8*lane+8); find the digit where the count
-      // from the top reaches `need`
-      int d[8], sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        d[i] = s_bins[lane * 8 + i];
-        sum += d[i];
-      }
-      int incl = sum;  // suffix sum over lanes
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += y;
-      }
-      int run = incl - sum;
-#pragma unroll
-      for (int i = 7; i >= 0; --i) {
-        if (run < need && run + d[i] >= need) {
-          s_digit = lane * 8 + i;
-          s_digit_above = run;
-          s_digit_count = d[i];
-        }
-        run += d[i];
-      }
-    }
-    __syncthreads();
-    need -= s_digit_above;
-    prefix = (prefix << 8) | (uint64_t)s_digit;
-    bits += 8;
-    const bool done = s_digit_count == need;
-    __syncthreads();
-    if (done) break;
-  }
-  const uint64_t kstar = bits == 64 ? prefix : (prefix << (64 - bits));
+  const uint64_t kstar = exact_threshold(cb, n, k - above, s_key, sm);
 
   if (len <= kBitmapTokens) {
     // ---- ordered output through the bitmap, staged in shared memory
@@ -348,7 +774,7 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
     int cnt = 0;
     for (int i = w0; i < w1; ++i) cnt += __popc(s_bm[i]);
     int tot;
-    int pos = block_exclusive_scan<kTopkThreads>(cnt, &tot, s_warp);
+    int pos = block_exclusive_scan<kTopkThreads>(cnt, &tot, sm.warp);
     for (int i = w0; i < w1; ++i) {
       uint32_t bits_w = s_bm[i];
       while (bits_w) {
@@ -384,7 +810,7 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
       if (cc < nch) mine += s_cnt[cc] + __ldcg(w.gt_cnt + (int64_t)b * nchunks_max + cc);
     }
     int tot;
-    int off = block_exclusive_scan<kTopkThreads>(mine, &tot, s_warp);
+    int off = block_exclusive_scan<kTopkThreads>(mine, &tot, sm.warp);
     for (int i = 0; i < per; ++i) {
       const int cc = tid * per + i;
       if (cc < nch) {
@@ -434,13 +860,13 @@ k_topk_emit(const int32_t* __restrict__ seq_lens, const uint32_t* __restrict__ b
 
 }  // namespace
 
-cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
-                        cudaStream_t s) {
-  const int max_len = a.max_pages * a.page_size;
-  dim3 grid(L.nchunks, a.B);
+namespace {
+
+TopkWs topk_ws(const WorkspaceLayout& L, uint8_t* ws) {
   TopkWs w;
   w.hist = reinterpret_cast<int32_t*>(ws + L.hist);
   w.tick = reinterpret_cast<int32_t*>(ws + L.tick_topk);
+  w.depart = reinterpret_cast<int32_t*>(ws + L.depart_topk);
   w.cand_n = reinterpret_cast<int32_t*>(ws + L.cand_n);
   w.cand = reinterpret_cast<int2*>(ws + L.cand);
   w.bits = reinterpret_cast<uint32_t*>(ws + L.bits);
@@ -448,6 +874,57 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
   w.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
   w.thr = reinterpret_cast<TopkThreshold*>(ws + L.thresh);
   w.err = reinterpret_cast<int32_t*>(ws + L.err);
+  return w;
+}
+
+// CTAs of k_topk_select the current device holds at once (cached per device).
+int64_t select_capacity() {
+  static int64_t cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int64_t& cap = cache[dev & 63];
+  if (cap == 0) {
+    int coop = 0, bps = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, k_topk_select, kTopkThreads, 0) !=
+            cudaSuccess)
+      bps = 0;
+    cap = coop ? (int64_t)bps * device_sm_count() : 0;
+    if (cap == 0) cap = -1;
+  }
+  return cap;
+}
+
+}  // namespace
+
+bool topk_single_launch(const pks_decode_args& a, const WorkspaceLayout& L) {
+  return a.topk_mode == 0 && L.nchunks <= kTopkCoopMaxChunks &&
+         (int64_t)L.nchunks * a.B <= select_capacity();
+}
+
+cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
+                        cudaStream_t s) {
+  const int max_len = a.max_pages * a.page_size;
+  const dim3 grid(L.nchunks, a.B);
+  const TopkWs w = topk_ws(L, ws);
+  const int32_t* scores = reinterpret_cast<const int32_t*>(ws + L.scores);
+  if (topk_single_launch(a, L)) {
+    // cooperative: the launch fails rather than run with CTAs of a request
+    // that cannot all be resident
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_topk_select, a.seq_lens, scores, L.ld, w,
+                              reinterpret_cast<int2*>(ws + L.chunk_cnt), a.topk_idx, a.k, max_len,
+                              (int)L.nchunks);
+  }
   const size_t smem = sizeof(uint64_t) * kCandCap + kBitmapTokens / 8 + sizeof(int) * L.nchunks;
   static size_t configured[64] = {0};
   int dev = 0;
@@ -459,9 +936,8 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
     if (e != cudaSuccess) return e;
     done = smem;
   }
-  k_topk_threshold<<<grid, kTopkThreads, smem, s>>>(
-      a.seq_lens, reinterpret_cast<const int32_t*>(ws + L.scores), L.ld, w, a.topk_idx, a.k,
-      max_len, L.nchunks);
+  k_topk_threshold<<<grid, kTopkThreads, smem, s>>>(a.seq_lens, scores, L.ld, w, a.topk_idx, a.k,
+                                                    max_len, L.nchunks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || max_len <= kBitmapTokens) return e;
   k_topk_emit<<<grid, kTopkThreads, 0, s>>>(
@@ -470,7 +946,8 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
   return cudaGetLastError();
 }
 
-int topk_kernel_launches(const pks_decode_args& a) {
+int topk_kernel_launches(const pks_decode_args& a, const WorkspaceLayout& L) {
+  if (topk_single_launch(a, L)) return 1;
   return (int64_t)a.max_pages * a.page_size > kBitmapTokens ? 2 : 1;
 }
 

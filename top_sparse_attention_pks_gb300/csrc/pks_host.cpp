@@ -48,7 +48,8 @@ pks_status check_shapes(const pks_decode_args* a) {
       a->attn_splits < 0 || a->attn_splits > kAttnGridMax)
     return PKS_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return PKS_ERR_INVALID;
-  if (a->reserved[0] || a->reserved[1] || a->reserved[2]) return PKS_ERR_INVALID;
+  if (a->topk_mode < 0 || a->topk_mode > 1) return PKS_ERR_INVALID;
+  if (a->reserved[0] || a->reserved[1]) return PKS_ERR_INVALID;
   if ((int64_t)a->num_pages * a->page_size > INT32_MAX) return PKS_ERR_UNSUPPORTED;
   if (a->D != 64 && a->D != 128) return PKS_ERR_UNSUPPORTED;
   if (a->Di != 64 && a->Di != 128) return PKS_ERR_UNSUPPORTED;
@@ -94,8 +95,10 @@ WorkspaceLayout workspace_layout(const pks_decode_args& a) {
   WorkspaceLayout L{};
   const int64_t B = a.B;
   const int G = a.Hq / a.Hkv;
-  L.ld = (int64_t)a.max_pages * a.page_size;
-  L.nchunks = (int)std::max<int64_t>(1, (L.ld + kTopkChunk - 1) / kTopkChunk);
+  const int64_t max_len = (int64_t)a.max_pages * a.page_size;
+  L.nchunks = (int)std::max<int64_t>(1, (max_len + kTopkChunk - 1) / kTopkChunk);
+  // score rows padded to whole top-k chunks, so chunk loads never leave the row
+  L.ld = (int64_t)L.nchunks * kTopkChunk;
 
   L.attn_grid_max = kAttnGridMax;
   const int hg = attn_heads_per_cta(a.Hkv);
@@ -111,12 +114,14 @@ WorkspaceLayout workspace_layout(const pks_decode_args& a) {
   L.err = take(sizeof(int32_t) * 4);
   L.hist = take(sizeof(int32_t) * (size_t)B * kScoreBins);
   L.tick_topk = take(sizeof(int32_t) * (size_t)B);
+  L.depart_topk = take(sizeof(int32_t) * (size_t)B);
   L.cand_n = take(sizeof(int32_t) * (size_t)B);
   L.ctrl_end = off;
   L.scores = take(sizeof(int32_t) * (size_t)B * (size_t)L.ld);
   L.cand = take(sizeof(int32_t) * 2 * (size_t)B * (size_t)L.ld);
   L.bits = take(sizeof(uint32_t) * (size_t)B * L.nchunks * (kTopkChunk / 32));
   L.gt_cnt = take(sizeof(int32_t) * (size_t)B * L.nchunks);
+  L.chunk_cnt = take(sizeof(int32_t) * 2 * (size_t)B * L.nchunks);
   L.chunk_off = take(sizeof(int32_t) * (size_t)B * L.nchunks);
   L.thresh = take(sizeof(TopkThreshold) * (size_t)B);
   L.attn_prefix = take(sizeof(int32_t) * (size_t)(B + 1));
@@ -334,6 +339,15 @@ static pks_status decode_impl(const pks_decode_args* args, pks_stream stream,
 
 pks_status pks_decode_step(const pks_decode_args* args, pks_stream stream) {
   return decode_impl(args, stream, nullptr);
+}
+
+pks_status pks_decode_launches(const pks_decode_args* args, int32_t* launches) {
+  if (!launches) return PKS_ERR_INVALID;
+  pks_status st = pks::check_shapes(args);
+  if (st != PKS_OK) return st;
+  const WorkspaceLayout L = pks::workspace_layout(*args);
+  *launches = args->B == 0 ? 0 : 1 + pks::topk_kernel_launches(*args, L) + 2;
+  return PKS_OK;
 }
 
 pks_status pks_decode_step_timed(const pks_decode_args* args, pks_stream stream,

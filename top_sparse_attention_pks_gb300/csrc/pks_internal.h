@@ -15,8 +15,10 @@ namespace pks {
 // 32 bins per power of two (about 2% wide); positives above 1024, negatives
 // mirrored below.
 constexpr int kScoreBins = 2048;
-// Tokens per top-k chunk (one CTA of the threshold and emit kernels).
+// Tokens per top-k chunk (one CTA of the top-k kernels).
 constexpr int kTopkChunk = 4096;
+// Most chunks per request the single-launch top-k handles.
+constexpr int kTopkCoopMaxChunks = 1024;
 // Attention: tokens per pipeline tile; largest persistent grid the workspace
 // holds partials for.
 constexpr int kAttnTile = 16;
@@ -49,10 +51,10 @@ struct TopkThreshold {
 // starts on a 256-byte boundary.  The control block (error word, histograms,
 // tickets, counters) must be zero between steps; everything else is scratch.
 struct WorkspaceLayout {
-  size_t ctrl, err, hist, tick_topk, cand_n, ctrl_end;
-  size_t scores, cand, bits, gt_cnt, chunk_off, thresh, attn_prefix, part_ml, part_o;
+  size_t ctrl, err, hist, tick_topk, depart_topk, cand_n, ctrl_end;
+  size_t scores, cand, bits, gt_cnt, chunk_cnt, chunk_off, thresh, attn_prefix, part_ml, part_o;
   size_t total;
-  int64_t ld;          // score row stride (max_pages * page_size)
+  int64_t ld;          // score row stride: max_pages * page_size rounded up to kTopkChunk
   int32_t nchunks;       // top-k chunks per request
   int32_t attn_grid_max; // attention CTAs the partial slots are sized for
 };
@@ -64,9 +66,11 @@ cudaError_t launch_indexer_scan(const pks_decode_args& a, int32_t* scores, int64
                                 int32_t* hist, int32_t* err, cudaStream_t s);
 cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
                         cudaStream_t s);
-// kernels launch_topk enqueues for these shapes (1, or 2 for contexts longer
-// than the shared-memory bitmap)
-int topk_kernel_launches(const pks_decode_args& a);
+// Top-k runs as one cooperative launch when all (chunk, request) CTAs fit on
+// the device at once; otherwise as the two-kernel fallback (threshold, plus
+// emit for contexts longer than the shared-memory bitmap).
+bool topk_single_launch(const pks_decode_args& a, const WorkspaceLayout& L);
+int topk_kernel_launches(const pks_decode_args& a, const WorkspaceLayout& L);
 // trim: the top-k list holds its selected entries first (the step's own
 // output), so only min(k, len_b) positions per request are visited.
 cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,

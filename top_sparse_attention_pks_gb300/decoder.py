@@ -15,7 +15,8 @@ class SparseDecodeStep:
     ``pks_decode_step`` on ``stream`` (default: torch's current stream).
     """
 
-    def __init__(self, tensors: dict, k: int, attn_splits: int = 0, stream=None):
+    def __init__(self, tensors: dict, k: int, attn_splits: int = 0, topk_mode: int = 0,
+                 stream=None):
         t = dict(tensors)
         q = t["q"]
         B, Hq, D = q.shape
@@ -25,13 +26,14 @@ class SparseDecodeStep:
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
         self.topk_idx = torch.empty((B, self.k), dtype=torch.int32, device=dev)
         probe = pks.make_args(k=self.k, topk_idx=self.topk_idx, out=self.out,
-                              attn_splits=attn_splits, **t)
+                              attn_splits=attn_splits, topk_mode=topk_mode, **t)
         nbytes = pks.pks_decode_workspace_size(probe)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         if self.workspace.data_ptr() % 256:
             raise RuntimeError("workspace allocation is not 256-byte aligned")
         self.args = pks.make_args(k=self.k, topk_idx=self.topk_idx, out=self.out,
-                                  workspace=self.workspace, attn_splits=attn_splits, **t)
+                                  workspace=self.workspace, attn_splits=attn_splits,
+                                  topk_mode=topk_mode, **t)
         pks.pks_decode_workspace_init(self.args, stream)
 
     def __call__(self, stream=None):
@@ -50,6 +52,10 @@ class SparseDecodeStep:
         out = torch.zeros((B, ld), dtype=torch.int32, device=self.out.device)
         pks.pks_indexer_scores(self.args, out, stream)
         return out
+
+    def launches(self) -> int:
+        """Kernels one step enqueues on the current device."""
+        return pks.pks_decode_launches(self.args)
 
     def device_error(self, stream=None) -> int:
         return pks.pks_decode_device_error(self.args, stream)

@@ -46,7 +46,8 @@ class pks_decode_args(ctypes.Structure):
         ("kv_k", ctypes.c_void_p), ("kv_v", ctypes.c_void_p), ("idx_k", ctypes.c_void_p),
         ("topk_idx", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("attn_splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3),
+        ("attn_splits", ctypes.c_int32), ("topk_mode", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -94,6 +95,8 @@ def _declare(L):
     L.pks_decode_workspace_init.restype = _ST
     L.pks_decode_step.argtypes = [_PARGS, _P]
     L.pks_decode_step.restype = _ST
+    L.pks_decode_launches.argtypes = [_PARGS, _P]
+    L.pks_decode_launches.restype = _ST
     L.pks_decode_step_timed.argtypes = [_PARGS, _P, _P]
     L.pks_decode_step_timed.restype = _ST
     L.pks_indexer_scores.argtypes = [_PARGS, _P, ctypes.c_int64, _P]
@@ -227,7 +230,7 @@ class Pool:
 
 def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: int,
               topk_idx=None, out=None, workspace=None, attn_splits: int = 0,
-              num_pages: Optional[int] = None) -> pks_decode_args:
+              topk_mode: int = 0, num_pages: Optional[int] = None) -> pks_decode_args:
     """Fill a ``pks_decode_args`` from tensors (shapes are read off the tensors)."""
     a = pks_decode_args()
     B, Hq, D = q.shape
@@ -256,6 +259,7 @@ def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: i
         a.workspace = _dptr(workspace, torch.uint8, "workspace")
         a.workspace_bytes = workspace.numel()
     a.attn_splits = int(attn_splits)
+    a.topk_mode = int(topk_mode)
     return a
 
 
@@ -269,6 +273,13 @@ def pks_decode_workspace_size(args: pks_decode_args) -> int:
 def pks_decode_workspace_init(args: pks_decode_args, stream=None) -> None:
     _check(lib().pks_decode_workspace_init(ctypes.byref(args), _stream(stream)),
            "pks_decode_workspace_init")
+
+
+def pks_decode_launches(args: pks_decode_args) -> int:
+    """Kernels one pks_decode_step with these shapes enqueues on the current device."""
+    n = ctypes.c_int32()
+    _check(lib().pks_decode_launches(ctypes.byref(args), ctypes.byref(n)), "pks_decode_launches")
+    return n.value
 
 
 def pks_decode_step(args: pks_decode_args, stream=None) -> None:
