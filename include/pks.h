@@ -63,6 +63,8 @@ typedef int32_t pks_status;
 #define PKS_ERR_DEVICE_CHECK (-5) /* a device-side bounds check fired (see *_device_error) */
 #define PKS_ERR_UNSUPPORTED (-6)  /* valid but outside the compiled shapes (see pks_decode_args) */
 #define PKS_ERR_WORKSPACE (-7)    /* workspace missing, misaligned or smaller than required */
+#define PKS_ERR_TOO_LARGE (-8)    /* shapes need more scratch than pks_sparse_attention_static's
+                                     fixed buffer holds */
 
 /* Static English text for a status code. */
 const char* pks_status_str(pks_status status);
@@ -187,6 +189,32 @@ pks_status pks_indexer_scores(const pks_decode_args* args, int32_t* scores, int6
  * (any order, -1 entries skipped, each position must be < len_b).  Writes
  * args->out; uses the workspace. */
 pks_status pks_sparse_attention(const pks_decode_args* args, pks_stream stream);
+
+/* pks_sparse_attention without a workspace, for callers that cannot allocate
+ * device memory: a runtime whose memory is planned ahead and locked, or code
+ * running where an allocation would synchronise or fail.  The sources have
+ * no counterpart of this call; it is a deployment convenience.  Same
+ * arguments, grid and results as pks_sparse_attention; args->workspace and
+ * workspace_bytes are ignored.
+ *
+ * Scratch: one file-scope device array of 8 MiB (8388608 bytes) inside
+ * libpks, holding the per-request position prefix and the split-K partials,
+ * (attention CTAs + (Hkv/hg)*B) * (Hq/Hkv)*hg * (D + 2) * 4 bytes (hg = the
+ * largest of 8, 4, 2, 1 dividing Hkv; CTAs = attn_splits, or the GPU's
+ * resident slots when 0).  TOO_LARGE when the shapes need more (checked on
+ * the host before any launch; nothing is enqueued).  The call makes no
+ * cudaMalloc, cudaFree or other allocating call, and nothing in the array has
+ * to start at zero: every word the merge reads is written earlier in the
+ * same call.
+ *
+ * Set-up: the first call on each device looks up the array's address with
+ * cudaGetSymbolAddress (that device current) and configures the kernels'
+ * shared-memory limits; make that first call outside any stream capture.
+ * The array is shared by every call on a device: calls that overlap in time
+ * (other streams, concurrent graph replays, other host threads) race on it.
+ * Device-side bounds checks skip bad rows as in pks_sparse_attention but are
+ * not reported (their flag lives in the array). */
+pks_status pks_sparse_attention_static(const pks_decode_args* args, pks_stream stream);
 
 /* Copy the workspace's device error word to *code (host) and clear it;
  * synchronises the stream.  *code = 0 when no device check fired, else the

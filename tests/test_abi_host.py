@@ -181,6 +181,16 @@ def test_workspace_size_and_validation_without_gpu():
     assert L.pks_indexer_scores(ctypes.byref(_cpu_args(idx_k=None)), None, 512, None) == -1
 
 
+def test_static_attention_rejects_oversized_shapes_on_host():
+    # the allocation-free attention checks its fixed scratch before any CUDA
+    # call: 4096 requests x 64 heads x 130 floats of partials exceed 8 MiB
+    import ctypes
+    a = _cpu_args()
+    a.B, a.Hq, a.Hkv, a.D = 4096, 64, 8, 128
+    assert pks.lib().pks_sparse_attention_static(ctypes.byref(a), None) == -8
+    assert pks.lib().pks_status_str(-8).decode().startswith("shapes need more scratch")
+
+
 def test_workspace_size_scales_with_batch():
     small = pks.pks_decode_workspace_size(_cpu_args())
     a = _cpu_args(B=50)

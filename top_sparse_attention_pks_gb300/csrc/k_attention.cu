@@ -536,6 +536,75 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
   return cudaGetLastError();
 }
 
+// ---- allocation-free variant: scratch in a fixed device array -------------
+// The attention scratch (the per-request position prefix, the device check
+// word and the split-K partials) lives in one file-scope device array instead
+// of a caller workspace.  Its size bounds the shapes: the partial slots grow
+// with (attention CTAs + head-group segments) x heads x D.
+__device__ __align__(256) uint8_t g_attn_static_scratch[kAttnStaticScratchBytes];
+
+// Scratch offsets inside the static array for `grid` attention CTAs.
+struct StaticAttnLayout {
+  size_t err, attn_prefix, part_ml, part_o, total;
+};
+StaticAttnLayout static_attn_layout(const pks_decode_args& a, int64_t grid) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const int hg = attn_heads_per_cta(a.Hkv);
+  const int G = a.Hq / a.Hkv;
+  const int64_t nseg = (int64_t)(a.Hkv / hg) * a.B;
+  const size_t nslots = (size_t)(grid + nseg) * hg * G;
+  StaticAttnLayout L{};
+  size_t off = 0;
+  L.err = off;
+  off = up(off + sizeof(int32_t) * 4);
+  L.attn_prefix = off;
+  off = up(off + sizeof(int32_t) * (size_t)(a.B + 1));
+  L.part_ml = off;
+  off = up(off + sizeof(float) * 2 * nslots);
+  L.part_o = off;
+  off = up(off + sizeof(float) * nslots * a.D);
+  L.total = off;
+  return L;
+}
+
+template <int D, int HG>
+cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cudaStream_t s,
+                                 bool* too_large) {
+  auto kern = k_sparse_attention<D, HG>;
+  const size_t smem = attn_smem_bytes<D, HG>(a.B);
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int bps = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, HG * 32, smem);
+  if (e != cudaSuccess) return e;
+  // the same grid pks_sparse_attention uses for these arguments
+  int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * (bps < 1 ? 1 : bps);
+  if (grid > kAttnGridMax) grid = kAttnGridMax;
+  const StaticAttnLayout L = static_attn_layout(a, grid);
+  if (L.total > kAttnStaticScratchBytes) {
+    *too_large = true;
+    return cudaSuccess;
+  }
+  const int G = a.Hq / a.Hkv;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
+  kern<<<grid, HG * 32, smem, s>>>(
+      a.seq_lens, a.block_table, reinterpret_cast<const __nv_bfloat16*>(a.q),
+      reinterpret_cast<const __nv_bfloat16*>(a.kv_k), reinterpret_cast<const __nv_bfloat16*>(a.kv_v),
+      a.topk_idx, reinterpret_cast<int32_t*>(scratch + L.attn_prefix),
+      reinterpret_cast<float2*>(scratch + L.part_ml), reinterpret_cast<float*>(scratch + L.part_o),
+      reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(scratch + L.err), a.B,
+      a.Hq, a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, /*trim=*/0, scale_log2);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_attention_merge<D><<<dim3((a.Hq + 3) / 4, a.B), 128, 0, s>>>(
+      reinterpret_cast<const int32_t*>(scratch + L.attn_prefix),
+      reinterpret_cast<const float2*>(scratch + L.part_ml),
+      reinterpret_cast<const float*>(scratch + L.part_o), reinterpret_cast<__nv_bfloat16*>(a.out),
+      a.B, a.Hq, a.Hkv, HG, G, grid);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
@@ -552,6 +621,44 @@ cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L,
   PKS_ATTN_CASE(128, 4)
   PKS_ATTN_CASE(128, 8)
 #undef PKS_ATTN_CASE
+  return cudaErrorInvalidValue;
+}
+
+size_t attention_static_min_bytes(const pks_decode_args& a) {
+  return static_attn_layout(a, 1).total;
+}
+
+cudaError_t attention_static_scratch(uint8_t** ptr) {
+  static void* cache[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev] = p;
+  }
+  *ptr = static_cast<uint8_t*>(cache[dev]);
+  return cudaSuccess;
+}
+
+cudaError_t launch_attention_static(const pks_decode_args& a, uint8_t* scratch, cudaStream_t s,
+                                    bool* too_large) {
+  *too_large = false;
+  const int hg = attn_heads_per_cta(a.Hkv);
+#define PKS_ATTN_STATIC_CASE(D_, HG_) \
+  if (a.D == D_ && hg == HG_) return launch_attn_static_t<D_, HG_>(a, scratch, s, too_large);
+  PKS_ATTN_STATIC_CASE(64, 1)
+  PKS_ATTN_STATIC_CASE(64, 2)
+  PKS_ATTN_STATIC_CASE(64, 4)
+  PKS_ATTN_STATIC_CASE(64, 8)
+  PKS_ATTN_STATIC_CASE(128, 1)
+  PKS_ATTN_STATIC_CASE(128, 2)
+  PKS_ATTN_STATIC_CASE(128, 4)
+  PKS_ATTN_STATIC_CASE(128, 8)
+#undef PKS_ATTN_STATIC_CASE
   return cudaErrorInvalidValue;
 }
 

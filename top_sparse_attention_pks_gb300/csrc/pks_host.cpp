@@ -162,6 +162,7 @@ const char* pks_status_str(pks_status status) {
     case PKS_ERR_DEVICE_CHECK: return "device-side bounds check failed";
     case PKS_ERR_UNSUPPORTED: return "unsupported shape";
     case PKS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PKS_ERR_TOO_LARGE: return "shapes need more scratch than the static buffer holds";
     default: return "unknown status";
   }
 }
@@ -385,6 +386,25 @@ pks_status pks_sparse_attention(const pks_decode_args* args, pks_stream stream) 
   return pks::from_cuda(pks::launch_attention(*args, L, static_cast<uint8_t*>(args->workspace),
                                               /*trim=*/false,
                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pks_status pks_sparse_attention_static(const pks_decode_args* args, pks_stream stream) {
+  pks_status st = pks::check_shapes(args);
+  if (st != PKS_OK) return st;
+  if ((st = pks::check_common_ptrs(args)) != PKS_OK) return st;
+  if ((st = pks::check_attn_ptrs(args)) != PKS_OK) return st;
+  // reject on the host, before any CUDA call, what cannot fit even with one CTA
+  if (pks::attention_static_min_bytes(*args) > pks::kAttnStaticScratchBytes)
+    return PKS_ERR_TOO_LARGE;
+  if (args->B == 0) return PKS_OK;
+  uint8_t* scratch = nullptr;
+  cudaError_t e = pks::attention_static_scratch(&scratch);
+  if (e != cudaSuccess) return PKS_ERR_CUDA;
+  bool too_large = false;
+  e = pks::launch_attention_static(*args, scratch, reinterpret_cast<cudaStream_t>(stream),
+                                   &too_large);
+  if (e != cudaSuccess) return PKS_ERR_CUDA;
+  return too_large ? PKS_ERR_TOO_LARGE : PKS_OK;
 }
 
 pks_status pks_decode_device_error(const pks_decode_args* args, int32_t* code,

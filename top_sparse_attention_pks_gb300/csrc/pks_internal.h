@@ -83,6 +83,17 @@ cudaError_t launch_residency(int32_t* state, int32_t num_pages, int32_t capacity
                              size_t off_flag, size_t off_slot_flag, size_t off_vict,
                              cudaStream_t s);
 
+// Allocation-free attention (pks_sparse_attention_static): bytes of the
+// file-scope device scratch array, the least any call with these shapes
+// needs (one attention CTA; host only), the array's address on the current
+// device (looked up once per device), and the launcher, which sets
+// *too_large instead of launching when the shapes need more than the array.
+constexpr size_t kAttnStaticScratchBytes = (size_t)8 << 20;
+size_t attention_static_min_bytes(const pks_decode_args& a);
+cudaError_t attention_static_scratch(uint8_t** ptr);
+cudaError_t launch_attention_static(const pks_decode_args& a, uint8_t* scratch, cudaStream_t s,
+                                    bool* too_large);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

@@ -24,6 +24,7 @@ STATUS_NAMES = {
     0: "PKS_OK", -1: "PKS_ERR_INVALID", -2: "PKS_ERR_OOM", -3: "PKS_ERR_CUDA",
     -4: "PKS_ERR_TIMEOUT", -5: "PKS_ERR_DEVICE_CHECK", -6: "PKS_ERR_UNSUPPORTED",
     -7: "PKS_ERR_WORKSPACE",
+    -8: "PKS_ERR_TOO_LARGE",
 }
 
 
@@ -95,6 +96,8 @@ def _declare(L):
     L.pks_decode_workspace_init.restype = _ST
     L.pks_decode_step.argtypes = [_PARGS, _P]
     L.pks_decode_step.restype = _ST
+    L.pks_sparse_attention_static.argtypes = [_PARGS, _P]
+    L.pks_sparse_attention_static.restype = _ST
     L.pks_decode_launches.argtypes = [_PARGS, _P]
     L.pks_decode_launches.restype = _ST
     L.pks_decode_step_timed.argtypes = [_PARGS, _P, _P]
@@ -304,6 +307,12 @@ def pks_indexer_scores(args: pks_decode_args, scores: torch.Tensor, stream=None)
 def pks_sparse_attention(args: pks_decode_args, stream=None) -> None:
     _check(lib().pks_sparse_attention(ctypes.byref(args), _stream(stream)),
            "pks_sparse_attention")
+
+
+def pks_sparse_attention_static(args: pks_decode_args, stream=None) -> None:
+    """Attention over args.topk_idx with the library's fixed device scratch (no workspace)."""
+    _check(lib().pks_sparse_attention_static(ctypes.byref(args), _stream(stream)),
+           "pks_sparse_attention_static")
 
 
 def pks_decode_device_error(args: pks_decode_args, stream=None) -> int:
