@@ -154,6 +154,9 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     if (tid == NT - 1) s_prefix[B] = before;
     __syncthreads();
   }
+  // the merge grid may take the SM slots this grid leaves free
+  pdl_launch_dependents();
+  pdl_wait();  // the selection comes from the top-k kernel
   const int64_t Treq = s_prefix[B];
   const int64_t T = Treq * ngroups;
   // with fewer positions than CTAs only the first T CTAs take part, so every
@@ -417,73 +420,91 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
 
 // Combine the partial (m, l, o) of a segment's contributing CTAs: one warp per
 // (query head, request); segments that one attention CTA owned whole are
-// skipped (it wrote the output itself).  Lanes split the contributors to find
-// the row's max and sum, then each lane accumulates float4 columns of o with
-// eight contributors' loads in flight at a time.
+// skipped (it wrote the output itself).  Two dependent L2 round trips: the
+// position prefix, then every contributor's (m, l) (one lane each) together
+// with the o rows of up to 16 contributors (lanes own float4 columns); more
+// contributors take further batches.
 template <int D>
 __global__ void __launch_bounds__(128)
 k_attention_merge(const int32_t* __restrict__ prefix, const float2* __restrict__ part_ml,
                   const float* __restrict__ part_o, __nv_bfloat16* __restrict__ out, int B,
                   int Hq, int Hkv, int HG, int G, int attn_grid) {
+  constexpr int DV4 = D / 4;  // float4 columns of a row (32 or 16)
+  constexpr int kBatch = 16;  // contributors' o rows in flight per lane
   const float kNegInf = __int_as_float(0xff800000);
   const int lane = threadIdx.x & 31;
   const int qh = blockIdx.x * 4 + (threadIdx.x >> 5);  // query head
   const int b = blockIdx.y;
+  pdl_wait();  // prefix and partials come from the attention kernel
   if (qh >= Hq) return;
   const int h = qh / G, gg = qh % G;  // KV head and row within its group
   const int g = h / HG, hh = h % HG;
   const int64_t Treq = prefix[B];
+  const int p0 = prefix[b], p1 = prefix[b + 1];
   const int64_t T = Treq * (Hkv / HG);
-  const int kb = prefix[b + 1] - prefix[b];
-  if (T == 0 || kb == 0) return;
+  if (T == 0 || p1 == p0) return;
   const int64_t GRID = T < (int64_t)attn_grid ? T : (int64_t)attn_grid;
-  const int64_t seg_lo = (int64_t)g * Treq + prefix[b];
-  const int c_first = owner_cta(seg_lo, T, GRID), c_last = owner_cta(seg_lo + kb - 1, T, GRID);
+  const int64_t seg_lo = (int64_t)g * Treq + p0;
+  const int c_first = owner_cta(seg_lo, T, GRID), c_last = owner_cta(seg_lo + (p1 - p0) - 1, T, GRID);
   if (c_first == c_last) return;
   const int seg = g * B + b;
   const int64_t pstride = (int64_t)HG * G;
   auto pidx = [&](int c) { return ((int64_t)c + seg) * pstride + (int64_t)hh * G + gg; };
+  const int nc = c_last - c_first + 1;
 
-  float M = kNegInf;
-  for (int c = c_first + lane; c <= c_last; c += 32) M = fmaxf(M, __ldcg(&part_ml[pidx(c)].x));
+  // (m, l) of contributors lane, lane + 32, ... and the first batch of o rows
+  float2 ml = nc > lane ? __ldcg(&part_ml[pidx(c_first + lane)]) : make_float2(kNegInf, 0.f);
+  float4 v[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u)
+    v[u] = (u < nc && lane < DV4)
+               ? __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c_first + u) * D) + lane)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  float M = ml.x;
+  for (int c = c_first + 32 + lane; c <= c_last; c += 32) M = fmaxf(M, __ldcg(&part_ml[pidx(c)].x));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float L = 0.f;
-  if (M != kNegInf)
-    for (int c = c_first + lane; c <= c_last; c += 32) {
-      const float2 ml = __ldcg(&part_ml[pidx(c)]);
-      if (ml.x != kNegInf) L += ml.y * exp2f(ml.x - M);
-    }
+  float L = ml.x == kNegInf ? 0.f : ml.y * exp2f(ml.x - M);
+  for (int c = c_first + 32 + lane; c <= c_last; c += 32) {
+    const float2 e = __ldcg(&part_ml[pidx(c)]);
+    if (e.x != kNegInf) L += e.y * exp2f(e.x - M);
+  }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float il = L > 0.f ? 1.f / L : 0.f;
+  // weight of contributor c_first + u (u < 32) from the lane holding its (m, l)
+  const float f_mine = ml.x == kNegInf ? 0.f : exp2f(ml.x - M);
 
-  constexpr int DV4 = D / 4;  // float4 columns of a row (32 or 16)
-  if (lane >= DV4) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = c_first; c0 <= c_last; c0 += 8) {
-    float m[8];
-    float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+  for (int u = 0; u < kBatch; ++u) {
+    const float f = __shfl_sync(0xffffffffu, f_mine, u);
+    acc.x += f * v[u].x;
+    acc.y += f * v[u].y;
+    acc.z += f * v[u].z;
+    acc.w += f * v[u].w;
+  }
+  for (int c0 = c_first + kBatch; c0 <= c_last; c0 += kBatch) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
       const int c = c0 + u;
-      if (c <= c_last) {
-        m[u] = __ldcg(&part_ml[pidx(c)].x);
-        v[u] = __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c) * D) + lane);
-      } else {
-        m[u] = kNegInf;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      v[u] = (c <= c_last && lane < DV4)
+                 ? __ldcg(reinterpret_cast<const float4*>(part_o + pidx(c) * D) + lane)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float f = m[u] == kNegInf ? 0.f : exp2f(m[u] - M);
+    for (int u = 0; u < kBatch; ++u) {
+      const int c = c0 + u;
+      float m = kNegInf;
+      if (c <= c_last) m = __ldcg(&part_ml[pidx(c)].x);
+      const float f = m == kNegInf ? 0.f : exp2f(m - M);
       acc.x += f * v[u].x;
       acc.y += f * v[u].y;
       acc.z += f * v[u].z;
       acc.w += f * v[u].w;
     }
   }
+  if (lane >= DV4) return;
   __nv_bfloat16* dst = out + ((int64_t)b * Hq + qh) * D + lane * 4;
   *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * il, acc.y * il);
   *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * il, acc.w * il);
@@ -520,20 +541,20 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
   if (grid > L.attn_grid_max) grid = L.attn_grid_max;
   const int G = a.Hq / a.Hkv;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
-  kern<<<grid, HG * 32, smem, s>>>(
-      a.seq_lens, a.block_table, reinterpret_cast<const __nv_bfloat16*>(a.q),
+  cudaError_t e = launch_ex(
+      kern, dim3(grid), dim3(HG * 32), smem, s, /*pdl=*/true, /*coop=*/false, a.seq_lens,
+      a.block_table, reinterpret_cast<const __nv_bfloat16*>(a.q),
       reinterpret_cast<const __nv_bfloat16*>(a.kv_k), reinterpret_cast<const __nv_bfloat16*>(a.kv_v),
-      a.topk_idx, reinterpret_cast<int32_t*>(ws + L.attn_prefix),
+      (const int32_t*)a.topk_idx, reinterpret_cast<int32_t*>(ws + L.attn_prefix),
       reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
       reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.B, a.Hq,
       a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, trim ? 1 : 0, scale_log2);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_attention_merge<D><<<dim3((a.Hq + 3) / 4, a.B), 128, 0, s>>>(
-      reinterpret_cast<const int32_t*>(ws + L.attn_prefix),
-      reinterpret_cast<const float2*>(ws + L.part_ml), reinterpret_cast<const float*>(ws + L.part_o),
-      reinterpret_cast<__nv_bfloat16*>(a.out), a.B, a.Hq, a.Hkv, HG, G, grid);
-  return cudaGetLastError();
+  return launch_ex(k_attention_merge<D>, dim3((a.Hq + 3) / 4, a.B), dim3(128), 0, s, true, false,
+                   reinterpret_cast<const int32_t*>(ws + L.attn_prefix),
+                   reinterpret_cast<const float2*>(ws + L.part_ml),
+                   reinterpret_cast<const float*>(ws + L.part_o),
+                   reinterpret_cast<__nv_bfloat16*>(a.out), a.B, a.Hq, a.Hkv, (int)HG, G, grid);
 }
 
 // ---- allocation-free variant: scratch in a fixed device array -------------

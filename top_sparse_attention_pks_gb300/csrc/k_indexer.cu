@@ -7,27 +7,24 @@
 // notes that selection needs the whole context resident in HBM: this kernel
 // streams every indexer key once and is bound by HBM bandwidth.
 //
-// Work split: the tokens of all requests are cut into rounds of 256 tokens of
-// one request; a persistent grid (one CTA per SM) gives each CTA a contiguous
-// range of rounds, and each of its 8 warps owns 32 tokens of every round.
-// A warp streams its tokens' keys with 16-byte cp.async (each warp-wide copy
-// covers 512 contiguous bytes when the tokens share a page) into its own
-// slice of a shared-memory ring several rounds deep, so HBM reads run well
-// ahead of the arithmetic and no block-wide barrier is needed in the loop.
-// Every lane then scores one token: it reads its key back from shared memory
-// (rows XOR-swizzled by 16-byte chunk, so the reads are conflict-free), runs
-// dp4a against the indexer query held in registers, applies ReLU and the
-// head weights.  Score stores are one 128-byte line per warp.
-
-#include <cuda.h>
+// Work split: the tokens of all requests are cut into CTA rounds of one
+// request; a persistent grid (one CTA per SM) gives each CTA a contiguous
+// range of rounds.  Keys stream from HBM straight into registers with
+// coalesced 16-byte loads (no shared-memory staging: on GB300 register
+// loads with 16+ warps an SM reach a higher read bandwidth than cp.async or
+// TMA fills of shared memory), one round ahead.  Two kernels:
+//  * 4 or 8 indexer heads: the head dot products are int8 tensor-core MMAs
+//    (k_indexer_scan_mma, 32 warps an SM);
+//  * 1 or 2 heads: dp4a with a transposed butterfly across the lanes of a
+//    token (k_indexer_scan_reg, 16 warps an SM).
+// Each score is binned into the request's shared-memory histogram, which is
+// added to the global one at the end (it seeds the top-k selection).
 
 #include "pks_internal.h"
 
 namespace pks {
 namespace {
 
-constexpr int kScanThreads = 256;
-constexpr int kRoundTokens = kScanThreads;
 
 __device__ __forceinline__ int score_bin(int s) {
   if (s == 0) return kScoreBins / 2;
@@ -71,252 +68,6 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_wa
   return before;
 }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-// Pipeline depth in rounds: 4 rounds of 32 KB (Di = 128) or 8 of 16 KB in
-// flight per CTA, enough to cover HBM latency at full bandwidth with one
-// CTA per SM.
-template <int DI>
-struct ScanCfg {
-  static constexpr int kStages = DI == 128 ? 5 : 9;
-  static constexpr int kStageBytes = kRoundTokens * DI;
-  static constexpr size_t smem_bytes(int B, int HI) {
-    return (size_t)kStages * kStageBytes + sizeof(int) * kScoreBins + 16 * (size_t)HI * (DI / 16) +
-           sizeof(int) * (size_t)(B + 1);
-  }
-};
-
-template <int HI, int DI>
-__global__ void __launch_bounds__(kScanThreads, 1)
-k_indexer_scan(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
-               const int8_t* __restrict__ q_idx, const int32_t* __restrict__ w_idx,
-               const int8_t* __restrict__ idx_k, int32_t* __restrict__ scores, int64_t ld,
-               int32_t* __restrict__ hist, int32_t* __restrict__ err, int B, int max_pages,
-               int page_size, int page_shift, int num_pages, int k) {
-  constexpr int CH = DI / 16;       // 16-byte chunks per key
-  constexpr int TPI = 32 / CH;      // tokens covered by one warp-wide load instruction
-  constexpr int SWZ_DIV = 8 / CH;   // chunk c of token r is stored at c ^ ((r / SWZ_DIV) % CH)
-  constexpr bool kQInRegs = HI <= 4;
-  constexpr int kStages = ScanCfg<DI>::kStages;
-  constexpr int kStageBytes = ScanCfg<DI>::kStageBytes;
-  constexpr int kWarpBytes = 32 * DI;
-
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;  // [kStages][8 warps][32 tokens][DI], rows swizzled by 16-byte chunk
-  int* s_hist = reinterpret_cast<int*>(smem + (size_t)kStages * kStageBytes);
-  int4* s_q = reinterpret_cast<int4*>(s_hist + kScoreBins);  // [HI][CH] when q is not in registers
-  int* s_prefix = reinterpret_cast<int*>(s_q + HI * CH);      // [B + 1] rounds prefix
-  __shared__ int s_warp[kScanThreads / 32];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int max_len = max_pages * page_size;
-
-  // rounds per request -> exclusive prefix in shared memory
-  const int per = (B + kScanThreads - 1) / kScanThreads;
-  int local = 0;
-  for (int i = 0; i < per; ++i) {
-    const int b = tid * per + i;
-    if (b < B) {
-      int len = seq_lens[b];
-      if (len < 0 || len > max_len) {
-        if (blockIdx.x == 0) flag_error(err, kErrLen);
-        len = 0;
-      }
-      local += (len + kRoundTokens - 1) / kRoundTokens;
-    }
-  }
-  int total_rounds;
-  int run = block_exclusive_scan<kScanThreads>(local, &total_rounds, s_warp);
-  for (int i = 0; i < per; ++i) {
-    const int b = tid * per + i;
-    if (b < B) {
-      s_prefix[b] = run;
-      int len = seq_lens[b];
-      if (len < 0 || len > max_len) len = 0;
-      run += (len + kRoundTokens - 1) / kRoundTokens;
-    }
-  }
-  if (tid == 0) s_prefix[B] = total_rounds;
-  for (int i = tid; i < kScoreBins; i += kScanThreads) s_hist[i] = 0;
-  __syncthreads();
-
-  const int64_t G = gridDim.x;
-  const int begin = (int)((int64_t)blockIdx.x * total_rounds / G);
-  const int end = (int)((int64_t)(blockIdx.x + 1) * total_rounds / G);
-  if (begin >= end) return;
-
-  // first request holding round `begin`
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_prefix[mid] <= begin) lo = mid; else hi = mid - 1;
-  }
-
-  // ---- loader.  Page lookups run two rounds ahead of the copies that use
-  // them (a dependent block-table read would otherwise stall the warp once
-  // per round).  lookup(item) returns this lane's physical token row, or -1.
-  int lk_b = lo, lk_len = 0;
-  {
-    const int len = seq_lens[lk_b];
-    lk_len = (len < 0 || len > max_len) ? 0 : len;
-  }
-  auto lookup_page = [&](int item, int& slot) -> int {
-    // advance to the request holding `item` (items only increase)
-    while (s_prefix[lk_b + 1] <= item) {
-      ++lk_b;
-      const int len = seq_lens[lk_b];
-      lk_len = (len < 0 || len > max_len) ? 0 : len;
-    }
-    const int t = (item - s_prefix[lk_b]) * kRoundTokens + warp * 32 + lane;
-    slot = -1;
-    if (t >= lk_len) return -1;
-    const int lp = page_shift >= 0 ? (t >> page_shift) : t / page_size;
-    slot = page_shift >= 0 ? (t & (page_size - 1)) : t % page_size;
-    return __ldg(block_table + (int64_t)lk_b * max_pages + lp);
-  };
-  auto issue = [&](int page, int slot, int stage) {
-    int row = -1;
-    if (slot >= 0) {
-      if ((unsigned)page < (unsigned)num_pages) row = page * page_size + slot;
-      else flag_error(err, kErrPage);
-    }
-    uint8_t* wbase = ring + (size_t)stage * kStageBytes + warp * kWarpBytes;
-    const int c = lane % CH;
-#pragma unroll
-    for (int i = 0; i < CH; ++i) {
-      const int tt = i * TPI + lane / CH;  // token of this warp's slice
-      const int rr = __shfl_sync(0xffffffffu, row, tt);
-      if (rr >= 0)
-        cp_async16(smem_u32(wbase + tt * DI + ((c ^ ((tt / SWZ_DIV) % CH)) << 4)),
-                   idx_k + (int64_t)rr * DI + c * 16);
-    }
-  };
-
-  // prologue: copies for the first kStages-1 rounds, lookups for the next two
-#pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
-    if (begin + st < end) {
-      int slot;
-      const int page = lookup_page(begin + st, slot);
-      issue(page, slot, st);
-    }
-    cp_async_commit();
-  }
-  int pg0 = -1, sl0 = -1, pg1 = -1, sl1 = -1;  // lookups of rounds begin+S-1, begin+S
-  if (begin + kStages - 1 < end) pg0 = lookup_page(begin + kStages - 1, sl0);
-  if (begin + kStages < end) pg1 = lookup_page(begin + kStages, sl1);
-
-  // ---- consumer: every lane scores one token per round
-  int4 q[kQInRegs ? HI : 1][kQInRegs ? CH : 1];
-  int w[HI];
-  int cb = -1, cb_len = 0;
-  bool do_hist = false;
-  int b = lo;
-  const int swz = (lane / SWZ_DIV) % CH;
-  for (int item = begin; item < end; ++item) {
-    const int rel = item - begin;
-    {
-      int pg2 = -1, sl2 = -1;
-      if (item + kStages + 1 < end) pg2 = lookup_page(item + kStages + 1, sl2);
-      if (item + kStages - 1 < end) issue(pg0, sl0, (rel + kStages - 1) % kStages);
-      pg0 = pg1;
-      sl0 = sl1;
-      pg1 = pg2;
-      sl1 = sl2;
-    }
-    cp_async_commit();
-
-    while (s_prefix[b + 1] <= item) ++b;
-    if (b != cb) {
-      // request switch (uniform across the CTA): flush the histogram, load q
-      if (do_hist) {
-        __syncthreads();
-        int32_t* gh = hist + (int64_t)cb * kScoreBins;
-        for (int i = tid; i < kScoreBins; i += kScanThreads) {
-          const int cnt = s_hist[i];
-          if (cnt) {
-            atomicAdd(gh + i, cnt);
-            s_hist[i] = 0;
-          }
-        }
-      }
-      __syncthreads();
-      cb = b;
-      const int len = seq_lens[b];
-      cb_len = (len < 0 || len > max_len) ? 0 : len;
-      do_hist = hist != nullptr && cb_len > k;
-      const int4* qg = reinterpret_cast<const int4*>(q_idx + (int64_t)b * HI * DI);
-      if constexpr (kQInRegs) {
-#pragma unroll
-        for (int h = 0; h < HI; ++h)
-#pragma unroll
-          for (int cc = 0; cc < CH; ++cc) q[h][cc] = __ldg(qg + h * CH + cc);
-      } else {
-        for (int i = tid; i < HI * CH; i += kScanThreads) s_q[i] = __ldg(qg + i);
-        __syncthreads();
-      }
-#pragma unroll
-      for (int h = 0; h < HI; ++h) w[h] = __ldg(w_idx + h);
-    }
-
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const uint8_t* rowp = ring + (size_t)(rel % kStages) * kStageBytes + warp * kWarpBytes + lane * DI;
-    int acc[HI];
-#pragma unroll
-    for (int h = 0; h < HI; ++h) acc[h] = 0;
-#pragma unroll
-    for (int cc = 0; cc < CH; ++cc) {
-      const int4 kv = *reinterpret_cast<const int4*>(rowp + ((cc ^ swz) << 4));
-#pragma unroll
-      for (int h = 0; h < HI; ++h) {
-        int4 qv;
-        if constexpr (kQInRegs) qv = q[h][cc];
-        else qv = s_q[h * CH + cc];
-        acc[h] = __dp4a(kv.x, qv.x, acc[h]);
-        acc[h] = __dp4a(kv.y, qv.y, acc[h]);
-        acc[h] = __dp4a(kv.z, qv.z, acc[h]);
-        acc[h] = __dp4a(kv.w, qv.w, acc[h]);
-      }
-    }
-    int score = 0;
-#pragma unroll
-    for (int h = 0; h < HI; ++h) score += w[h] * max(acc[h], 0);
-
-    const int t = (item - s_prefix[b]) * kRoundTokens + warp * 32 + lane;
-    const bool valid = t < cb_len;
-    if (valid) scores[(int64_t)b * ld + t] = score;
-    if (do_hist) {
-      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-      if (valid) {
-        const int bin = score_bin(score);
-        const unsigned peers = __match_any_sync(vmask, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
-      }
-    }
-    __syncwarp();
-  }
-  cp_async_wait<0>();
-  if (do_hist) {
-    __syncthreads();
-    int32_t* gh = hist + (int64_t)cb * kScoreBins;
-    for (int i = tid; i < kScoreBins; i += kScanThreads) {
-      const int cnt = s_hist[i];
-      if (cnt) atomicAdd(gh + i, cnt);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Register-streaming variant.  Keys go from HBM straight into registers with
 // coalesced 16-byte loads (each warp-wide load covers Di/16 lanes x 32/(Di/16)
@@ -345,6 +96,8 @@ k_indexer_scan_reg(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   constexpr int NI = LPT;        // loads per lane per round (32 tokens)
 
   extern __shared__ int smem_i[];
+  // the top-k grid may take SM slots as soon as this grid's CTAs retire
+  pdl_launch_dependents();
   int* s_hist = smem_i;                 // [kScoreBins]
   int* s_prefix = smem_i + kScoreBins;  // [B + 1]
   __shared__ int s_warp[kRegThreads / 32];
@@ -570,6 +323,8 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   constexpr int NLD = 2 * 2 * HALVES;  // loads per lane per 32-token round
 
   extern __shared__ int smem_i[];
+  // the top-k grid may take SM slots as soon as this grid's CTAs retire
+  pdl_launch_dependents();
   int* s_hist = smem_i;                 // [kScoreBins]
   int* s_prefix = smem_i + kScoreBins;  // [B + 1]
   __shared__ int s_warp[NT / 32];
@@ -749,346 +504,6 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   }
 }
 
-// ---------------------------------------------------------------------------
-// TMA variant (page sizes that are powers of two >= 8).  Same work split; the
-// copies are tiled cp.async.bulk.tensor loads of one box of min(64, page_size)
-// key rows, issued by one lane per box, completing on a per-warp, per-stage
-// mbarrier.  The 128-byte (Di = 128) or 64-byte (Di = 64) swizzle of the
-// tensor map puts chunk c of row r at c ^ (r % 8) or c ^ ((r / 2) % 4): the
-// layout the readers use.  8 warps per CTA (one CTA per SM); a warp round is
-// 64 tokens and every lane scores two of them (rows lane and lane + 32), so
-// each indexer-query load and all per-round bookkeeping serve two tokens.
-
-constexpr int kTmaWarps = 8;
-constexpr int kTmaThreads = kTmaWarps * 32;
-constexpr int kWarpTokens = 64;
-constexpr int kTmaRound = kTmaWarps * kWarpTokens;  // tokens per CTA round
-constexpr uint32_t kWaitLimit = 1u << 24;           // bounded mbarrier wait (polls)
-
-template <int DI>
-struct TmaCfg {
-  static constexpr int kStages = DI == 128 ? 3 : 6;
-  static constexpr int kWarpStage = kWarpTokens * DI;  // bytes of one warp's round
-  static size_t smem_bytes(int B, int HI) {
-    return 1024 + (size_t)kTmaWarps * kStages * kWarpStage + sizeof(int) * kScoreBins +
-           (size_t)HI * DI + sizeof(uint64_t) * kTmaWarps * kStages + sizeof(int) * (size_t)(B + 1);
-  }
-};
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false if the phase did not complete within kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-template <int HI, int DI>
-__global__ void __launch_bounds__(kTmaThreads, 1)
-k_indexer_scan_tma(const __grid_constant__ CUtensorMap keys, const int32_t* __restrict__ seq_lens,
-                   const int32_t* __restrict__ block_table, const int8_t* __restrict__ q_idx,
-                   const int32_t* __restrict__ w_idx, int32_t* __restrict__ scores, int64_t ld,
-                   int32_t* __restrict__ hist, int32_t* __restrict__ err, int B, int max_pages,
-                   int page_size, int page_shift, int num_pages, int k) {
-  constexpr int CH = DI / 16;
-  constexpr int SWZ_DIV = 8 / CH;
-  constexpr int kStages = TmaCfg<DI>::kStages;
-  constexpr int kWarpStage = TmaCfg<DI>::kWarpStage;
-  constexpr bool kQInRegs = HI * CH <= 16;
-
-  extern __shared__ uint8_t smem_raw[];
-  // the swizzle pattern is taken from address bits: align the ring to 1 KB
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* ring = smem;  // [warps][kStages][64 rows][DI]
-  int* s_hist = reinterpret_cast<int*>(ring + (size_t)kTmaWarps * kStages * kWarpStage);
-  int4* s_q = reinterpret_cast<int4*>(s_hist + kScoreBins);                // [HI][CH]
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_q + HI * CH);           // [warps][kStages]
-  int* s_prefix = reinterpret_cast<int*>(s_bar + kTmaWarps * kStages);    // [B + 1]
-  __shared__ int s_warp[kTmaThreads / 32];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int max_len = max_pages * page_size;
-  const int box_rows = page_size < kWarpTokens ? page_size : kWarpTokens;
-  const int nbox = kWarpTokens / box_rows;  // boxes per warp round (<= 8)
-
-  // rounds per request -> exclusive prefix in shared memory
-  const int per = (B + kTmaThreads - 1) / kTmaThreads;
-  int local = 0;
-  for (int i = 0; i < per; ++i) {
-    const int b = tid * per + i;
-    if (b < B) {
-      int len = seq_lens[b];
-      if (len < 0 || len > max_len) {
-        if (blockIdx.x == 0) flag_error(err, kErrLen);
-        len = 0;
-      }
-      local += (len + kTmaRound - 1) / kTmaRound;
-    }
-  }
-  int total_rounds;
-  int run = block_exclusive_scan<kTmaThreads>(local, &total_rounds, s_warp);
-  for (int i = 0; i < per; ++i) {
-    const int b = tid * per + i;
-    if (b < B) {
-      s_prefix[b] = run;
-      int len = seq_lens[b];
-      if (len < 0 || len > max_len) len = 0;
-      run += (len + kTmaRound - 1) / kTmaRound;
-    }
-  }
-  if (tid == 0) s_prefix[B] = total_rounds;
-  for (int i = tid; i < kScoreBins; i += kTmaThreads) s_hist[i] = 0;
-  if (lane == 0)
-    for (int st = 0; st < kStages; ++st) mbar_init(smem_u32(&s_bar[warp * kStages + st]), 1);
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  __syncthreads();
-
-  const int64_t G = gridDim.x;
-  const int begin = (int)((int64_t)blockIdx.x * total_rounds / G);
-  const int end = (int)((int64_t)(blockIdx.x + 1) * total_rounds / G);
-  if (begin >= end) return;
-
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_prefix[mid] <= begin) lo = mid; else hi = mid - 1;
-  }
-
-  // ---- producer side.  Lane i < nbox owns box i of the warp's 64 tokens;
-  // page lookups run two rounds ahead of the copies.
-  int lk_b = lo, lk_len = 0, lk_next = s_prefix[lo + 1];
-  {
-    const int len = seq_lens[lk_b];
-    lk_len = (len < 0 || len > max_len) ? 0 : len;
-  }
-  // -> first row of this lane's box in the key pool, or -1 (no box)
-  auto lookup_box = [&](int item) -> int {
-    while (lk_next <= item) {
-      ++lk_b;
-      lk_next = s_prefix[lk_b + 1];
-      const int len = seq_lens[lk_b];
-      lk_len = (len < 0 || len > max_len) ? 0 : len;
-    }
-    const int t0 = (item - s_prefix[lk_b]) * kTmaRound + warp * kWarpTokens + lane * box_rows;
-    if (lane >= nbox || t0 >= lk_len) return -1;
-    const int page = __ldg(block_table + (int64_t)lk_b * max_pages + (t0 >> page_shift));
-    if ((unsigned)page >= (unsigned)num_pages) {
-      flag_error(err, kErrPage);
-      return -1;
-    }
-    return page * page_size + (t0 & (page_size - 1));
-  };
-  uint8_t* wring = ring + (size_t)warp * kStages * kWarpStage;
-  const uint32_t bar0 = smem_u32(&s_bar[warp * kStages]);
-  auto produce = [&](int row, int stage) {
-    const uint32_t bar = bar0 + 8u * stage;
-    const unsigned have = __ballot_sync(0xffffffffu, row >= 0);
-    if (lane == 0) mbar_arrive_tx(bar, (uint32_t)__popc(have) * box_rows * DI);
-    __syncwarp();
-    if (row >= 0)
-      tma_load_2d(smem_u32(wring + (size_t)stage * kWarpStage + (size_t)lane * box_rows * DI),
-                  &keys, 0, row, bar);
-  };
-
-  int pst = 0;  // stage the next produce goes to
-#pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
-    if (begin + st < end) produce(lookup_box(begin + st), pst);
-    pst = pst + 1 == kStages ? 0 : pst + 1;
-  }
-  int rw0 = -1, rw1 = -1;  // looked-up boxes of rounds begin+S-1 and begin+S
-  if (begin + kStages - 1 < end) rw0 = lookup_box(begin + kStages - 1);
-  if (begin + kStages < end) rw1 = lookup_box(begin + kStages);
-
-  // ---- consumer side: every lane scores rows lane and lane + 32 of a round
-  int4 q[kQInRegs ? HI : 1][kQInRegs ? CH : 1];
-  int w[HI];
-  int cb = -1, cb_len = 0, cb_first = 0, cb_next = 0;
-  bool do_hist = false, dead = false;
-  int cst = 0;       // stage being consumed
-  uint32_t par = 0;  // its mbarrier phase parity
-  const int swz = (lane / SWZ_DIV) % CH;  // same for rows lane and lane + 32
-  for (int item = begin; item < end; ++item) {
-    {
-      const int rw2 = item + kStages + 1 < end ? lookup_box(item + kStages + 1) : -1;
-      if (item + kStages - 1 < end && !dead) produce(rw0, pst);
-      pst = pst + 1 == kStages ? 0 : pst + 1;
-      rw0 = rw1;
-      rw1 = rw2;
-    }
-
-    if (item >= cb_next) {
-      // request switch (uniform across the CTA): flush the histogram, load q
-      int b = cb < 0 ? lo : cb;
-      while (s_prefix[b + 1] <= item) ++b;
-      if (do_hist) {
-        __syncthreads();
-        int32_t* gh = hist + (int64_t)cb * kScoreBins;
-        for (int i = tid; i < kScoreBins; i += kTmaThreads) {
-          const int cnt = s_hist[i];
-          if (cnt) {
-            atomicAdd(gh + i, cnt);
-            s_hist[i] = 0;
-          }
-        }
-      }
-      __syncthreads();
-      cb = b;
-      cb_first = s_prefix[b];
-      cb_next = s_prefix[b + 1];
-      const int len = seq_lens[b];
-      cb_len = (len < 0 || len > max_len) ? 0 : len;
-      do_hist = hist != nullptr && cb_len > k;
-      const int4* qg = reinterpret_cast<const int4*>(q_idx + (int64_t)b * HI * DI);
-      if constexpr (kQInRegs) {
-#pragma unroll
-        for (int h = 0; h < HI; ++h)
-#pragma unroll
-          for (int cc = 0; cc < CH; ++cc) q[h][cc] = __ldg(qg + h * CH + cc);
-      } else {
-        for (int i = tid; i < HI * CH; i += kTmaThreads) s_q[i] = __ldg(qg + i);
-        __syncthreads();
-      }
-#pragma unroll
-      for (int h = 0; h < HI; ++h) w[h] = __ldg(w_idx + h);
-    }
-
-    if (!dead && !mbar_wait(bar0 + 8u * cst, par)) {
-      flag_error(err, kErrTimeout);
-      dead = true;
-    }
-    __syncwarp();
-    const uint8_t* row0 = wring + (size_t)cst * kWarpStage + lane * DI;
-    const uint8_t* row1 = row0 + 32 * DI;
-    int acc0[HI], acc1[HI];
-#pragma unroll
-    for (int h = 0; h < HI; ++h) acc0[h] = acc1[h] = 0;
-#pragma unroll
-    for (int cc = 0; cc < CH; ++cc) {
-      const int4 k0 = *reinterpret_cast<const int4*>(row0 + ((cc ^ swz) << 4));
-      const int4 k1 = *reinterpret_cast<const int4*>(row1 + ((cc ^ swz) << 4));
-#pragma unroll
-      for (int h = 0; h < HI; ++h) {
-        int4 qv;
-        if constexpr (kQInRegs) qv = q[h][cc];
-        else qv = s_q[h * CH + cc];
-        acc0[h] = __dp4a(k0.x, qv.x, acc0[h]);
-        acc1[h] = __dp4a(k1.x, qv.x, acc1[h]);
-        acc0[h] = __dp4a(k0.y, qv.y, acc0[h]);
-        acc1[h] = __dp4a(k1.y, qv.y, acc1[h]);
-        acc0[h] = __dp4a(k0.z, qv.z, acc0[h]);
-        acc1[h] = __dp4a(k1.z, qv.z, acc1[h]);
-        acc0[h] = __dp4a(k0.w, qv.w, acc0[h]);
-        acc1[h] = __dp4a(k1.w, qv.w, acc1[h]);
-      }
-    }
-    int s0 = 0, s1 = 0;
-#pragma unroll
-    for (int h = 0; h < HI; ++h) {
-      s0 += w[h] * max(acc0[h], 0);
-      s1 += w[h] * max(acc1[h], 0);
-    }
-    cst = cst + 1 == kStages ? 0 : cst + 1;
-    par ^= cst == 0 ? 1u : 0u;
-
-    const int t0 = (item - cb_first) * kTmaRound + warp * kWarpTokens + lane;
-    const bool v0 = t0 < cb_len && !dead, v1 = t0 + 32 < cb_len && !dead;
-    int32_t* srow = scores + (int64_t)cb * ld;
-    if (v0) srow[t0] = s0;
-    if (v1) srow[t0 + 32] = s1;
-    if (do_hist) {
-      const unsigned m0 = __ballot_sync(0xffffffffu, v0);
-      if (v0) {
-        const int bin = score_bin(s0);
-        const unsigned peers = __match_any_sync(m0, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
-      }
-      const unsigned m1 = __ballot_sync(0xffffffffu, v1);
-      if (v1) {
-        const int bin = score_bin(s1);
-        const unsigned peers = __match_any_sync(m1, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
-      }
-    }
-    __syncwarp();
-  }
-  if (dead) {
-    // let this warp's copies still in flight land before the CTA exits
-    for (int st = 0; st < kStages; ++st) (void)mbar_wait(bar0 + 8u * st, 0);
-  }
-  if (do_hist) {
-    __syncthreads();
-    int32_t* gh = hist + (int64_t)cb * kScoreBins;
-    for (int i = tid; i < kScoreBins; i += kTmaThreads) {
-      const int cnt = s_hist[i];
-      if (cnt) atomicAdd(gh + i, cnt);
-    }
-  }
-}
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// Tensor map over the key pool viewed as [num_pages * page_size rows, Di bytes].
-bool make_key_map(const pks_decode_args& a, CUtensorMap* map) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)a.Di, (cuuint64_t)a.num_pages * a.page_size};
-  const cuuint64_t strides[1] = {(cuuint64_t)a.Di};
-  const cuuint32_t box[2] = {(cuuint32_t)a.Di,
-                             (cuuint32_t)(a.page_size < kWarpTokens ? a.page_size : kWarpTokens)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(a.idx_k), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            a.Di == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Raise a kernel's dynamic shared-memory limit once per device to the
-// largest size seen.  `configured` must belong to that one kernel.  Not a
-// stream operation, so after the first call it stays out of graph capture.
 template <typename K>
 cudaError_t raise_smem(K kern, size_t smem, size_t (&configured)[64]) {
   int dev = 0;
@@ -1103,6 +518,8 @@ cudaError_t raise_smem(K kern, size_t smem, size_t (&configured)[64]) {
   return cudaSuccess;
 }
 
+constexpr int kMmaThreads = 1024;
+
 template <int HI, int DI>
 cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld, int32_t* hist,
                           int32_t* err, cudaStream_t s) {
@@ -1112,19 +529,21 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
     while ((1 << shift) < a.page_size) ++shift;
   }
   static size_t configured[64] = {0};  // per instantiation
-  // 4 or 8 heads: int8 MMA; 1 or 2 heads: dp4a
-  constexpr int kMmaThreads = 1024;
-  auto kern = HI >= 4 ? k_indexer_scan_mma<(HI >= 4 ? HI : 4), DI, kMmaThreads>
-                      : k_indexer_scan_reg<HI, DI>;
-  const int threads = HI >= 4 ? kMmaThreads : kRegThreads;
   const size_t smem = sizeof(int) * ((size_t)kScoreBins + a.B + 1);
-  cudaError_t e = raise_smem(kern, smem, configured);
-  if (e != cudaSuccess) return e;
-  kern<<<device_sm_count(), threads, smem, s>>>(a.seq_lens, a.block_table, a.q_idx, a.w_idx,
-                                                    a.idx_k, scores, ld, hist, err, a.B,
-                                                    a.max_pages, a.page_size, shift, a.num_pages,
-                                                    a.k);
-  return cudaGetLastError();
+  auto go = [&](auto kern, int threads) {
+    cudaError_t e = raise_smem(kern, smem, configured);
+    if (e != cudaSuccess) return e;
+    kern<<<device_sm_count(), threads, smem, s>>>(a.seq_lens, a.block_table, a.q_idx, a.w_idx,
+                                                  a.idx_k, scores, ld, hist, err, a.B,
+                                                  a.max_pages, a.page_size, shift, a.num_pages,
+                                                  a.k);
+    return cudaGetLastError();
+  };
+  // 4 or 8 heads: int8 MMA; 1 or 2 heads: dp4a
+  if constexpr (HI >= 4)
+    return go(k_indexer_scan_mma<HI, DI, kMmaThreads>, kMmaThreads);
+  else
+    return go(k_indexer_scan_reg<HI, DI>, kRegThreads);
 }
 
 }  // namespace

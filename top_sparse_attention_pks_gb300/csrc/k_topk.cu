@@ -461,9 +461,11 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int start = c * kTopkChunk;
+  const int len = clamp_len(seq_lens[b], max_len);
+  pdl_wait();  // scores and histogram come from the scan
 
   // all loads of the chunk phase at once: scores (rows padded to whole
-  // chunks, so always in bounds), the histogram and the length
+  // chunks, so always in bounds) and the histogram
   int4 v[kRounds];
   {
     const int4* sp = reinterpret_cast<const int4*>(scores + (int64_t)b * ld + start);
@@ -479,7 +481,6 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
     h[0] = h0.x; h[1] = h0.y; h[2] = h0.z; h[3] = h0.w;
     h[4] = h1.x; h[5] = h1.y; h[6] = h1.z; h[7] = h1.w;
   }
-  const int len = clamp_len(seq_lens[b], max_len);
   int32_t* row = topk + (int64_t)b * k;
   if (len <= k) {
     const int nch = max(1, (len + kTopkChunk - 1) / kTopkChunk);
@@ -565,6 +566,9 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
     if (tid == 0) atomicCAS(w.err, 0, kErrTimeout);
     return;
   }
+  // every CTA of the request is resident: the attention grid may now take
+  // SM slots without keeping a CTA of this grid from its barrier
+  pdl_launch_dependents();
   // every CTA has read the histogram: clear it for the next step
   if (c == 0)
     for (int i = tid; i < kScoreBins; i += kTopkThreads) hb[i] = 0;
@@ -720,6 +724,8 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
 
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   const int len = clamp_len(seq_lens[b], max_len);
+  pdl_wait();  // scores and histogram come from the scan
+  pdl_launch_dependents();
   int32_t* row = topk + (int64_t)b * k;
   if (len <= k) {
     const int nch = max(1, (len + kTopkChunk - 1) / kTopkChunk);
@@ -840,6 +846,8 @@ k_topk_emit(const int32_t* __restrict__ seq_lens, const uint32_t* __restrict__ b
   constexpr int kWords = kTopkChunk / 32;  // 128 words per chunk
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   const int len = clamp_len(seq_lens[b], max_len);
+  pdl_wait();  // bitmap and offsets come from k_topk_threshold
+  pdl_launch_dependents();
   if (len <= k || len <= kBitmapTokens) return;  // written by the threshold kernel
   const int nch = (len + kTopkChunk - 1) / kTopkChunk;
   if (c >= nch) return;
@@ -911,19 +919,9 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
   if (topk_single_launch(a, L)) {
     // cooperative: the launch fails rather than run with CTAs of a request
     // that cannot all be resident
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kTopkThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_topk_select, a.seq_lens, scores, L.ld, w,
-                              reinterpret_cast<int2*>(ws + L.chunk_cnt), a.topk_idx, a.k, max_len,
-                              (int)L.nchunks);
+    return launch_ex(k_topk_select, grid, dim3(kTopkThreads), 0, s, /*pdl=*/true, /*coop=*/true,
+                     a.seq_lens, scores, L.ld, w, reinterpret_cast<int2*>(ws + L.chunk_cnt),
+                     a.topk_idx, a.k, max_len, (int)L.nchunks);
   }
   const size_t smem = sizeof(uint64_t) * kCandCap + kBitmapTokens / 8 + sizeof(int) * L.nchunks;
   static size_t configured[64] = {0};
@@ -936,14 +934,14 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
     if (e != cudaSuccess) return e;
     done = smem;
   }
-  k_topk_threshold<<<grid, kTopkThreads, smem, s>>>(a.seq_lens, scores, L.ld, w, a.topk_idx, a.k,
-                                                    max_len, L.nchunks);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_ex(k_topk_threshold, grid, dim3(kTopkThreads), smem, s, true, false,
+                            a.seq_lens, scores, L.ld, w, a.topk_idx, a.k, max_len,
+                            (int)L.nchunks);
   if (e != cudaSuccess || max_len <= kBitmapTokens) return e;
-  k_topk_emit<<<grid, kTopkThreads, 0, s>>>(
-      a.seq_lens, reinterpret_cast<const uint32_t*>(ws + L.bits),
-      reinterpret_cast<const int32_t*>(ws + L.chunk_off), a.topk_idx, a.k, max_len, L.nchunks);
-  return cudaGetLastError();
+  return launch_ex(k_topk_emit, grid, dim3(kTopkThreads), 0, s, true, false, a.seq_lens,
+                   reinterpret_cast<const uint32_t*>(ws + L.bits),
+                   reinterpret_cast<const int32_t*>(ws + L.chunk_off), a.topk_idx, a.k, max_len,
+                   (int)L.nchunks);
 }
 
 int topk_kernel_launches(const pks_decode_args& a, const WorkspaceLayout& L) {

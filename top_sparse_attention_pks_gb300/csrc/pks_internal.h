@@ -7,7 +7,49 @@
 
 #include "pks.h"
 
+#include <utility>
+
 namespace pks {
+
+// ---- programmatic dependent launch (PDL) ----
+// The kernels of a step after the first are launched with programmatic
+// stream serialisation: their CTAs may be scheduled while the previous
+// kernel drains, run what does not depend on it, and wait in pdl_wait()
+// until it has completed and its writes are visible.  A kernel calls
+// pdl_launch_dependents() once the next kernel's CTAs may take SM slots.
+// Both are no-ops for a kernel launched without the attribute.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+#endif
+
+// cudaLaunchKernelEx with optional PDL and cooperative attributes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t s, bool pdl, bool coop, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (coop) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- indexer score histogram (fused into the scan, consumed by top-k) ----
 // 2048 bins over int32 scores, order preserving: 0 -> bin 1024; |s| > 0 is
