@@ -311,7 +311,7 @@ __device__ __forceinline__ void imma_16832(int (&c)[4], int a0, int a1, int a2, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int HI, int DI, int NT>
+template <int HI, int DI, int NT, bool DB>
 __global__ void __launch_bounds__(NT, 1)
 k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                    const int8_t* __restrict__ q_idx, const int32_t* __restrict__ w_idx,
@@ -412,11 +412,25 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
       }
   };
 
-  // single-buffered: the other warps of the SM overlap a warp's load latency
-  int4 cur[NLD];
-  int pg0, sl0, pg1, sl1;  // lookups of rounds item and item+1
-  pg0 = lookup(begin, sl0);
-  pg1 = begin + 1 < end ? lookup(begin + 1, sl1) : (sl1 = -1, -1);
+  // page lookups run two rounds ahead of the loads that use them
+  int pg0, sl0, pg1, sl1;  // lookups of the next two rounds to load
+  int next_lookup = begin;
+  pg0 = lookup(next_lookup, sl0);
+  ++next_lookup;
+  pg1 = next_lookup < end ? lookup(next_lookup, sl1) : (sl1 = -1, -1);
+  ++next_lookup;
+  // row of this lane's token in the next round to load
+  auto next_row = [&]() -> int {
+    const int row = to_row(pg0, sl0);
+    int sl2 = -1;
+    const int pg2 = next_lookup < end ? lookup(next_lookup, sl2) : -1;
+    ++next_lookup;
+    pg0 = pg1;
+    sl0 = sl1;
+    pg1 = pg2;
+    sl1 = sl2;
+    return row;
+  };
 
   int4 qf[HALVES];  // chunks 4*hv + tq of head gq (zero for padded heads)
   int w0 = 0, w1 = 0;  // weights of heads 2tq and 2tq+1
@@ -424,16 +438,8 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   bool do_hist = false;
   // output token of this lane: tile (tq >> 1), row gq + 8 * (tq & 1)
   const int my_tok = (tq >> 1) * 16 + gq + 8 * (tq & 1);
-  for (int item = begin; item < end; ++item) {
-    load_round(to_row(pg0, sl0), cur);
-    {
-      int sl2 = -1;
-      const int pg2 = item + 2 < end ? lookup(item + 2, sl2) : -1;
-      pg0 = pg1;
-      sl0 = sl1;
-      pg1 = pg2;
-      sl1 = sl2;
-    }
+  // scores of round `item` from its keys in buf
+  auto process = [&](int item, const int4 (&buf)[NLD]) {
     if (item >= cb_next) {
       int b = cb < 0 ? lo : cb;
       while (s_prefix[b + 1] <= item) ++b;
@@ -470,8 +476,8 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
       int c[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int hv = 0; hv < HALVES; ++hv) {
-        const int4 r0 = cur[(u * HALVES + hv) * 2 + 0];  // token row gq
-        const int4 r1 = cur[(u * HALVES + hv) * 2 + 1];  // token row gq + 8
+        const int4 r0 = buf[(u * HALVES + hv) * 2 + 0];  // token row gq
+        const int4 r1 = buf[(u * HALVES + hv) * 2 + 1];  // token row gq + 8
         imma_16832<DI>(c, r0.x, r1.x, r0.y, r1.y, qf[hv].x, qf[hv].y);
         imma_16832<DI>(c, r0.z, r1.z, r0.w, r1.w, qf[hv].z, qf[hv].w);
       }
@@ -493,6 +499,27 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     // plain shared atomics: colliding lanes of a warp are serialised by the
     // hardware, which costs less than aggregating them first
     if (do_hist && valid) atomicAdd(&s_hist[score_bin(score)], 1);
+  };
+
+  if constexpr (DB) {
+    // ping-pong: round i+1 loads into one buffer while round i computes from
+    // the other, and round i+2's loads go out before round i+1 is awaited
+    int4 ba[NLD], bb[NLD];
+    load_round(next_row(), ba);
+    for (int item = begin; item < end; item += 2) {
+      if (item + 1 < end) load_round(next_row(), bb);
+      process(item, ba);
+      if (item + 1 >= end) break;
+      if (item + 2 < end) load_round(next_row(), ba);
+      process(item + 1, bb);
+    }
+  } else {
+    // single-buffered: the other warps of the SM overlap a warp's load latency
+    int4 cur[NLD];
+    for (int item = begin; item < end; ++item) {
+      load_round(next_row(), cur);
+      process(item, cur);
+    }
   }
   if (do_hist) {
     __syncthreads();
@@ -518,7 +545,9 @@ cudaError_t raise_smem(K kern, size_t smem, size_t (&configured)[64]) {
   return cudaSuccess;
 }
 
+// int8-MMA scan: threads a CTA (one CTA an SM) and double buffering
 constexpr int kMmaThreads = 1024;
+constexpr bool kMmaDoubleBuffer = false;
 
 template <int HI, int DI>
 cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld, int32_t* hist,
@@ -541,7 +570,7 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
   };
   // 4 or 8 heads: int8 MMA; 1 or 2 heads: dp4a
   if constexpr (HI >= 4)
-    return go(k_indexer_scan_mma<HI, DI, kMmaThreads>, kMmaThreads);
+    return go(k_indexer_scan_mma<HI, DI, kMmaThreads, kMmaDoubleBuffer>, kMmaThreads);
   else
     return go(k_indexer_scan_reg<HI, DI>, kRegThreads);
 }

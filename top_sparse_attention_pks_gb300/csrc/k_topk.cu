@@ -338,23 +338,50 @@ __device__ __forceinline__ void write_dense(int32_t* row, int len, int k, int c)
 
 // Single-launch selection for grids that fit on the GPU at once (launched
 // cooperatively, so all CTAs of a request are resident together).  One CTA
-// per (4096-token chunk, request); thread i owns the 4 consecutive tokens
-// 4i..4i+3 of each of the chunk's 4 rounds of 1024 tokens, read with one
-// 16-byte load per round (score rows are padded to whole chunks).
-//  1. Chunk phase: threshold bin T1 from the histogram; per-thread masks of
-//     the tokens above T1 and in T1; the chunk's T1 tokens go to the chunk's
-//     own region of the candidate buffer and its two counts to chunk_cnt
-//     (no atomics).
+// per (4096-token chunk, request); thread i owns the 16 consecutive tokens
+// 16i..16i+15 of the chunk, read with four 16-byte loads (score rows are
+// padded to whole chunks).
+//  1. Chunk phase: threshold bin T1 from the histogram and the score range
+//     [lo, hi] of that bin; per-thread masks of the tokens above hi and in
+//     [lo, hi]; the chunk's T1 tokens go to the chunk's own region of the
+//     candidate buffer and its two counts to chunk_cnt (no atomics).
 //  2. Counter barrier of the request's CTAs.
-//  3. Every CTA gathers all candidates of the request (chunk order), selects
-//     the same exact threshold key, and writes its own chunk's selected
-//     tokens in ascending order at the chunk's output offset: tokens above T1
-//     in earlier chunks plus selected candidates of earlier chunks.
+//  3. Every CTA reads all chunks' counts together with the first candidates
+//     of every chunk (one round trip), selects the same exact threshold key,
+//     and writes its own chunk's selected tokens in ascending order at the
+//     chunk's output offset: tokens above T1 in earlier chunks plus selected
+//     candidates of earlier chunks.
 // CTA 0 clears the histogram once every CTA has read it; the last CTA to
 // leave resets the request's barrier counters.
-constexpr int kVec = 4;                                          // tokens per load
-constexpr int kRounds = kTopkChunk / (kTopkThreads * kVec);      // 4
-constexpr int kSlices = kRounds * (kTopkThreads / 32);           // 32 (round, warp) slices
+constexpr int kTokPerThread = kTopkChunk / kTopkThreads;  // 16
+constexpr int kSpecSlots = 2 * kTopkThreads;              // candidates read with the counts
+
+// Score range [lo, hi] of a non-empty histogram bin (the inverse of
+// score_bin on the scores that reach the bin).
+__device__ __forceinline__ void bin_range(int bin, int& lo, int& hi) {
+  if (bin == kScoreBins / 2) {
+    lo = hi = 0;
+    return;
+  }
+  const bool pos = bin > kScoreBins / 2;
+  const int v = pos ? bin - (kScoreBins / 2 + 1) : (kScoreBins / 2 - 1) - bin;
+  const int e = v >> 5, m = v & 31;
+  int64_t alo, ahi;
+  if (e >= 5) {
+    alo = (int64_t)(32 + m) << (e - 5);
+    ahi = ((int64_t)(33 + m) << (e - 5)) - 1;
+  } else {
+    alo = (32 + m) >> (5 - e);
+    ahi = alo;
+  }
+  if (pos) {
+    lo = (int)alo;
+    hi = (int)(ahi > INT32_MAX ? (int64_t)INT32_MAX : ahi);
+  } else {
+    lo = (int)(-ahi < (int64_t)INT32_MIN ? (int64_t)INT32_MIN : -ahi);
+    hi = (int)(-alo);
+  }
+}
 
 template <typename KeyAt>
 __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_at,
@@ -455,22 +482,20 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
               int k, int max_len, int nchunks_max) {
   __shared__ uint64_t s_key[kCandCap];
   __shared__ int s_eqoff[kTopkCoopMaxChunks + 1];  // candidates before each chunk
-  __shared__ int s_slice[kSlices];
-  __shared__ int s_before;
+  __shared__ int s_before, s_lo, s_hi;
   __shared__ TopkSmem sm;
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
   const int start = c * kTopkChunk;
   const int len = clamp_len(seq_lens[b], max_len);
   pdl_wait();  // scores and histogram come from the scan
 
-  // all loads of the chunk phase at once: scores (rows padded to whole
-  // chunks, so always in bounds) and the histogram
-  int4 v[kRounds];
+  // all loads of the chunk phase at once: this thread's 16 scores (rows
+  // padded to whole chunks, so always in bounds) and 8 histogram bins
+  int4 v[4];
   {
-    const int4* sp = reinterpret_cast<const int4*>(scores + (int64_t)b * ld + start);
+    const int4* sp = reinterpret_cast<const int4*>(scores + (int64_t)b * ld + start) + 4 * tid;
 #pragma unroll
-    for (int r = 0; r < kRounds; ++r) v[r] = __ldcg(sp + r * kTopkThreads + tid);
+    for (int r = 0; r < 4; ++r) v[r] = __ldcg(sp + r);
   }
   int32_t* hb = w.hist + (int64_t)b * kScoreBins;
   constexpr int kPer = kScoreBins / kTopkThreads;  // 8 bins a thread
@@ -510,6 +535,10 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
       if (run < k && run + h[i] >= k) {
         sm.T1 = tid * kPer + i;
         sm.above = run;
+        int lo, hi;
+        bin_range(tid * kPer + i, lo, hi);
+        s_lo = lo;
+        s_hi = hi;
       }
       run += h[i];
     }
@@ -522,37 +551,37 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
     if (tid == 0 && c == 0) atomicCAS(w.err, 0, kErrState);
     return;
   }
+  const int lo = s_lo, hi = s_hi;
 
-  // ---- masks of this thread's tokens above T1 (gtm) and in T1 (eqm);
-  // bit r*4+e is token start + r*1024 + 4*tid + e
+  // ---- masks of this thread's tokens above T1 (gtm) and in T1 (eqm); bit j
+  // is token start + 16 * tid + j
   unsigned gtm = 0, eqm = 0;
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
+  for (int r = 0; r < 4; ++r) {
     const int sv[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-      const int t = start + r * (kTopkThreads * kVec) + tid * kVec + e;
-      const int bin = score_bin(sv[e]);
-      const bool valid = t < stop;
-      gtm |= (unsigned)(valid && bin > T1) << (r * kVec + e);
-      eqm |= (unsigned)(valid && bin == T1) << (r * kVec + e);
+    for (int e = 0; e < 4; ++e) {
+      const int bit = 4 * r + e;
+      const bool valid = start + kTokPerThread * tid + bit < stop;
+      gtm |= (unsigned)(valid && sv[e] > hi) << bit;
+      eqm |= (unsigned)(valid && sv[e] >= lo && sv[e] <= hi) << bit;
     }
   }
   // one scan of both counts: above-T1 in the high half, candidates in the low
   int packed_total;
   const int packed_before = block_exclusive_scan<kTopkThreads>(
       (__popc(gtm) << 16) | __popc(eqm), &packed_total, sm.warp);
-  int2* cregion = w.cand + ((int64_t)b * nchunks_max + c) * kTopkChunk;
   const int eq_before = packed_before & 0xffff;
+  int2* cregion = w.cand + ((int64_t)b * nchunks_max + c) * kTopkChunk;
   if (eqm) {
     int pos = eq_before;
 #pragma unroll
-    for (int r = 0; r < kRounds; ++r) {
+    for (int r = 0; r < 4; ++r) {
       const int sv[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
 #pragma unroll
-      for (int e = 0; e < kVec; ++e)
-        if ((eqm >> (r * kVec + e)) & 1u)
-          cregion[pos++] = make_int2(sv[e], start + r * (kTopkThreads * kVec) + tid * kVec + e);
+      for (int e = 0; e < 4; ++e)
+        if ((eqm >> (4 * r + e)) & 1u)
+          cregion[pos++] = make_int2(sv[e], start + kTokPerThread * tid + 4 * r + e);
     }
   }
   if (tid == 0)
@@ -573,7 +602,18 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
   if (c == 0)
     for (int i = tid; i < kScoreBins; i += kTopkThreads) hb[i] = 0;
 
-  // ---- per-chunk counts -> candidate offsets and this chunk's above-T1 offset
+  // ---- per-chunk counts, read together with the first `win` candidates of
+  // every chunk (slots tid and tid + kTopkThreads)
+  const int2* cbase = w.cand + (int64_t)b * nchunks_max * kTopkChunk;
+  const int win = kSpecSlots / nch;  // 0 when there are more chunks than slots
+  int2 spec[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int slot = tid + u * kTopkThreads;
+    spec[u] = make_int2(0, -1);
+    if (win > 0 && slot / win < nch)
+      spec[u] = __ldcg(cbase + (int64_t)(slot / win) * kTopkChunk + slot % win);
+  }
   {
     // nch <= kTopkCoopMaxChunks = 4 * kTopkThreads: up to 4 chunks a thread,
     // their candidate counts parked in s_eqoff across the scan
@@ -604,21 +644,37 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
     __syncthreads();
   }
   const int n = s_eqoff[nch];
-  const int2* cbase = w.cand + (int64_t)b * nchunks_max * kTopkChunk;
-  // candidate i of the request, in chunk order
+  // candidate i of the request, in chunk order, from L2
   auto cand_at = [&](int i) -> int2 {
-    int lo = 0, hi = nch - 1;  // last chunk with s_eqoff <= i
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_eqoff[mid] <= i) lo = mid; else hi = mid - 1;
+    int l = 0, h2 = nch - 1;  // last chunk with s_eqoff <= i
+    while (l < h2) {
+      const int mid = (l + h2 + 1) >> 1;
+      if (s_eqoff[mid] <= i) l = mid; else h2 = mid - 1;
     }
-    return __ldcg(cbase + (int64_t)lo * kTopkChunk + (i - s_eqoff[lo]));
+    return __ldcg(cbase + (int64_t)l * kTopkChunk + (i - s_eqoff[l]));
   };
   const bool staged = n <= kCandCap;
   if (staged) {
+    // the speculatively read candidates, then the rest of any chunk with more
+    // than `win` of them
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int slot = tid + u * kTopkThreads;
+      if (win > 0 && slot / win < nch) {
+        const int ch = slot / win, jj = slot % win;
+        if (jj < s_eqoff[ch + 1] - s_eqoff[ch]) s_key[s_eqoff[ch] + jj] = order_key(spec[u].x, spec[u].y);
+      }
+    }
     for (int i = tid; i < n; i += kTopkThreads) {
-      const int2 e = cand_at(i);
-      s_key[i] = order_key(e.x, e.y);
+      int l = 0, h2 = nch - 1;
+      while (l < h2) {
+        const int mid = (l + h2 + 1) >> 1;
+        if (s_eqoff[mid] <= i) l = mid; else h2 = mid - 1;
+      }
+      if (i - s_eqoff[l] >= win) {
+        const int2 e = __ldcg(cbase + (int64_t)l * kTopkChunk + (i - s_eqoff[l]));
+        s_key[i] = order_key(e.x, e.y);
+      }
     }
     __syncthreads();
   }
@@ -634,55 +690,26 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
   for (int i = tid; i < s_eqoff[c]; i += kTopkThreads) before += key_at(i) >= kstar;
   before = s_before + block_sum<kTopkThreads>(before, sm.warp);
 
-  // ---- this chunk's selected tokens, ascending: round, warp, lane, element
-  // this thread's candidates sit in the request's list in token order from
-  // its chunk's offset plus its scan position
+  // ---- this chunk's selected tokens, ascending: this thread's candidates sit
+  // in the request's list in token order from its chunk's offset plus its
+  // scan position
   unsigned selm = gtm;
   if (eqm) {
     int i = s_eqoff[c] + eq_before;
 #pragma unroll
-    for (int bit = 0; bit < kRounds * kVec; ++bit)
+    for (int bit = 0; bit < kTokPerThread; ++bit)
       if ((eqm >> bit) & 1u) {
         if (key_at(i) >= kstar) selm |= 1u << bit;
         ++i;
       }
   }
-  const unsigned lt = (1u << lane) - 1u;
-  int lane_before[kRounds];  // selected tokens of lower lanes in this (round, warp) slice
-#pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const int mine = __popc((selm >> (r * kVec)) & 0xfu);
-    int x = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    lane_before[r] = x - mine;
-    if (lane == 31) s_slice[r * (kTopkThreads / 32) + warp] = x;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const int v0 = s_slice[lane];  // kSlices == 32: one slice a lane
-    int x = v0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    s_slice[lane] = x - v0;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    int pos = before + s_slice[r * (kTopkThreads / 32) + warp] + lane_before[r];
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-      if ((selm >> (r * kVec + e)) & 1u) {
-        if (pos < k) row[pos] = start + r * (kTopkThreads * kVec) + tid * kVec + e;
-        ++pos;
-      }
-    }
+  int sel_total;
+  int pos = before + block_exclusive_scan<kTopkThreads>(__popc(selm), &sel_total, sm.warp);
+  while (selm) {
+    const int bit = __ffs(selm) - 1;
+    selm &= selm - 1u;
+    if (pos < k) row[pos] = start + kTokPerThread * tid + bit;
+    ++pos;
   }
 
   // the last CTA to leave resets the request's barrier counters
