@@ -324,12 +324,7 @@ def main():
     if dist:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_s = sum(step_ms) / 1e3
-    if dist:
-        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_s = float(tt.item())
-    value = world * args.steps / total_s
+    value, total_s = job_throughput(sum(step_ms) / 1e3, args.steps, world, dist, dev)
     ms_per_step = total_s * 1e3 / args.steps
 
     # ---- per-stage times inside the real step (events between the stages)
@@ -390,6 +385,17 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def job_throughput(local_s, steps, world, dist=None, device="cpu"):
+    """Whole-job steps/s: every rank ran `steps` replica steps; the job took
+    as long as its slowest rank (max over ranks).  Returns (value, max_s)."""
+    total_s = float(local_s)
+    if dist is not None and world > 1:
+        tt = torch.tensor([total_s], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+    return world * steps / total_s, total_s
 
 
 def shrink(wl, n):

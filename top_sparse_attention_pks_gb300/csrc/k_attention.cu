@@ -6,18 +6,20 @@
 // page table, so the reads are scattered rows that the kernel must gather
 // efficiently.
 //
-// One CTA per (split, KV head, request).  A split is a contiguous range of
-// top-k positions.  The CTA first turns its positions into physical token rows
-// (block table lookup, bounds checked), then streams 64-token tiles of K and V
-// rows for its KV head (D*2 bytes each, contiguous) with 16-byte cp.async into
-// a 3-stage shared-memory ring; rows are stored XOR-swizzled by 16-byte chunk
-// so that ldmatrix reads are free of bank conflicts.  Each of the 4 warps owns
-// 16 tokens of every tile and keeps its own online-softmax state for the G
-// query heads of the group: S = Q K^T and O += P V run on the tensor cores
-// (bf16 in, fp32 accumulate) with the G heads as the 16-row M dimension,
-// padded with zero rows.  The warps' states are merged in shared memory, and
-// the splits of one (request, KV head) are merged by the last CTA to finish
-// (log-sum-exp rescaling), which writes the bf16 output.
+// Persistent stream-K over the flattened (KV-head group, request, selected
+// position) space: every CTA (one per SM) takes an equal contiguous range of
+// it.  A CTA first turns its positions into physical token rows (block table
+// lookup, bounds checked), then streams 16-token tiles of K and V rows for
+// its head group (HG heads x D x 2 bytes, contiguous) with 16-byte cp.async
+// into a 3-stage shared-memory ring; rows are stored XOR-swizzled by 16-byte
+// chunk so that ldmatrix reads are free of bank conflicts.  Each warp owns one
+// KV head and keeps an online-softmax state for the G query heads that share
+// it: S = Q K^T and O += P V run on the tensor cores (bf16 in, fp32
+// accumulate) with the G heads as the 16-row M dimension, padded with zero
+// rows.  A CTA that owns a whole (group, request) segment writes its bf16
+// output; otherwise it writes a partial (m, l, o) to a slot indexed by
+// (CTA + segment), and k_attention_merge combines the partials of each split
+// segment by log-sum-exp rescaling.
 //
 // At G = 8 query heads per KV head the work is about 8 FLOP per byte of K/V,
 // far below the tensor-core ridge: the kernel is bound by HBM bandwidth, and
