@@ -161,7 +161,7 @@ pks_status pks_decode_workspace_size(const pks_decode_args* args, size_t* bytes)
  * leaves them zero again, so steps can be replayed (e.g. in a CUDA graph). */
 pks_status pks_decode_workspace_init(const pks_decode_args* args, pks_stream stream);
 
-/* The whole step: scan, top-k, attention.  Three or four kernel launches:
+/* The whole step: scan, top-k, attention.  Four or more kernel launches:
  * scan, top-k, attention and merge; top-k is one cooperative launch when all
  * of its (4096-token chunk, request) CTAs fit on the device at once, else two
  * (three with more than 131072 tokens per request); see pks_decode_launches.

@@ -124,7 +124,7 @@ def test_long_request_emit_path(topk_mode):
     t, _, _ = prepare(wl)
     step, _, _ = full_check(wl, t, topk_mode=topk_mode)
     # scan + top-k (one cooperative launch, or threshold + emit) + attention + merge
-    assert step.launches() == (4 if topk_mode == 0 else 5)
+    assert step.launches() == (5 if topk_mode == 1 else 4)
 
 
 @pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])

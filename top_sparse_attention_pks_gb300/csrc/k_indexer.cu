@@ -35,6 +35,14 @@ __device__ __forceinline__ int score_bin(int s) {
   return s > 0 ? kScoreBins / 2 + 1 + v : kScoreBins / 2 - 1 - v;
 }
 
+// Score store with an L2 evict-last policy: the top-k reads the scores right
+// after the scan, while the keys stream through L2 with evict-first loads.
+__device__ __forceinline__ void store_score_keep(int32_t* p, int v) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+  asm volatile("st.global.L2::cache_hint.s32 [%0], %1, %2;\n" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ void flag_error(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -267,7 +275,7 @@ k_indexer_scan_reg(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     // lane (g, j) now holds token slot j, i.e. token j * TPI + g of the round
     const int t = (item - cb_first) * kRegRound + warp * 32 + j * TPI + g;
     const bool valid = t < cb_len;
-    if (valid) scores[(int64_t)cb * ld + t] = score;
+    if (valid) store_score_keep(scores + (int64_t)cb * ld + t, score);
     if (do_hist) {
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);
       if (valid) {
@@ -495,7 +503,7 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
                                 : ((tq & 1) ? sc[0][1] : sc[0][0]);  // no local-memory indexing
     const int t = (item - cb_first) * NT + warp * 32 + my_tok;
     const bool valid = t < cb_len;
-    if (valid) scores[(int64_t)cb * ld + t] = score;
+    if (valid) store_score_keep(scores + (int64_t)cb * ld + t, score);
     // plain shared atomics: colliding lanes of a warp are serialised by the
     // hardware, which costs less than aggregating them first
     if (do_hist && valid) atomicAdd(&s_hist[score_bin(score)], 1);

@@ -115,14 +115,16 @@ struct TopkWs {
 };
 
 // Shared memory of the chunk phase and the exact select.
-struct TopkSmem {
-  int warp[kTopkThreads / 32];
-  int bins[kTopkThreads];
+template <int NT>
+struct TopkSmemT {
+  int warp[NT / 32];
+  int bins[NT > 256 ? NT : 256];  // threshold-bin scan (NT), radix digits (256)
   int T1, above, flag;
   int digit, digit_above, digit_count;
   int cand_base;
-  unsigned long long kand[kTopkThreads / 32], kor[kTopkThreads / 32];
+  unsigned long long kand[NT / 32], kor[NT / 32];
 };
+using TopkSmem = TopkSmemT<kTopkThreads>;
 
 // Chunk phase, run by every CTA of a request: load the chunk's scores, find
 // the threshold bin T1 from the request's histogram, count the chunk's tokens
@@ -216,106 +218,15 @@ __device__ __forceinline__ bool chunk_phase(const int32_t* __restrict__ sb, cons
   return true;
 }
 
-// Exact threshold key among the n candidates: the need-th largest
-// (score, ~token) key, radix-selected 8 bits at a time after the leading bits
-// that every candidate shares.  Candidates are staged in s_key when they fit,
-// else re-read from the list in L2 on every pass.  Block-wide; every thread
-// returns the key.
-__device__ __forceinline__ uint64_t exact_threshold(const int2* cb, int n, int need,
-                                                    uint64_t* s_key, TopkSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool staged = n <= kCandCap;
-  uint64_t kand = ~0ull, kor = 0ull;
-  for (int i = tid; i < n; i += kTopkThreads) {
-    const int2 e = __ldcg(cb + i);
-    const uint64_t key = order_key(e.x, e.y);
-    if (staged) s_key[i] = key;
-    kand &= key;
-    kor |= key;
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    kand &= __shfl_xor_sync(0xffffffffu, kand, o);
-    kor |= __shfl_xor_sync(0xffffffffu, kor, o);
-  }
-  if (lane == 0) {
-    sm.kand[warp] = kand;
-    sm.kor[warp] = kor;
-  }
-  __syncthreads();
-  kand = ~0ull;
-  kor = 0ull;
-#pragma unroll
-  for (int i = 0; i < kTopkThreads / 32; ++i) {
-    kand &= sm.kand[i];
-    kor |= sm.kor[i];
-  }
-  const int common = n > 0 ? __clzll((long long)(kand ^ kor)) : 64;  // 64 when all equal
-  int bits = (common / 8) * 8;
-  uint64_t prefix = bits == 0 ? 0ull : (bits == 64 ? kand : (kand >> (64 - bits)));
-  while (bits < 64) {
-    const int shift = 56 - bits;
-    sm.bins[tid] = 0;
-    if (tid == 0) {
-      sm.digit = 0;
-      sm.digit_above = 0;
-      sm.digit_count = 0;
-    }
-    __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) {
-      uint64_t key;
-      if (staged) {
-        key = s_key[i];
-      } else {
-        const int2 e = __ldcg(cb + i);
-        key = order_key(e.x, e.y);
-      }
-      if (bits == 0 || (key >> (64 - bits)) == prefix)
-        atomicAdd(&sm.bins[(int)((key >> shift) & 255u)], 1);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane owns digits [8*lane, 8*lane+8); find the digit where the count
-      // from the top reaches `need`
-      int d[8], sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        d[i] = sm.bins[lane * 8 + i];
-        sum += d[i];
-      }
-      int incl = sum;  // suffix sum over lanes
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += y;
-      }
-      int run = incl - sum;
-#pragma unroll
-      for (int i = 7; i >= 0; --i) {
-        if (run < need && run + d[i] >= need) {
-          sm.digit = lane * 8 + i;
-          sm.digit_above = run;
-          sm.digit_count = d[i];
-        }
-        run += d[i];
-      }
-    }
-    __syncthreads();
-    need -= sm.digit_above;
-    prefix = (prefix << 8) | (uint64_t)sm.digit;
-    bits += 8;
-    const bool done = sm.digit_count == need;
-    __syncthreads();
-    if (done) break;
-  }
-  return bits == 64 ? prefix : (prefix << (64 - bits));
-}
-
-// Bounded wait until `count` CTAs of a request have arrived.  Called by one
-// thread after the CTA's writes are ordered by __syncthreads.
-__device__ __forceinline__ bool request_barrier(int32_t* arrive, int count) {
+// Arrival at a request barrier, by one thread after the CTA's writes are
+// ordered by __syncthreads.
+__device__ __forceinline__ void request_arrive(int32_t* arrive) {
   __threadfence();
   atomicAdd(arrive, 1);
+}
+
+// Bounded wait until `count` CTAs of a request have arrived (one thread).
+__device__ __forceinline__ bool request_wait(int32_t* arrive, int count) {
   for (int it = 0; it < kBarrierSpins; ++it) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(arrive) : "memory");
@@ -383,12 +294,16 @@ __device__ __forceinline__ void bin_range(int bin, int& lo, int& hi) {
   }
 }
 
-template <typename KeyAt>
+// Exact threshold key among the n candidates: the need-th largest
+// (score, ~token) key, radix-selected 8 bits at a time after the leading bits
+// that every candidate shares.  Block-wide (NT threads); every thread returns
+// the key.
+template <int NT, typename KeyAt>
 __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_at,
-                                                     TopkSmem& sm) {
+                                                     TopkSmemT<NT>& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint64_t kand = ~0ull, kor = 0ull;
-  for (int i = tid; i < n; i += kTopkThreads) {
+  for (int i = tid; i < n; i += NT) {
     const uint64_t key = key_at(i);
     kand &= key;
     kor |= key;
@@ -406,7 +321,7 @@ __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_
   kand = ~0ull;
   kor = 0ull;
 #pragma unroll
-  for (int i = 0; i < kTopkThreads / 32; ++i) {
+  for (int i = 0; i < NT / 32; ++i) {
     kand &= sm.kand[i];
     kor |= sm.kor[i];
   }
@@ -415,9 +330,9 @@ __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_
   uint64_t prefix = bits == 0 ? 0ull : (bits == 64 ? kand : (kand >> (64 - bits)));
   while (bits < 64) {
     const int shift = 56 - bits;
-    sm.bins[tid] = 0;
+    if (tid < 256) sm.bins[tid] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) {
+    for (int i = tid; i < n; i += NT) {
       const uint64_t key = key_at(i);
       if (bits == 0 || (key >> (64 - bits)) == prefix)
         atomicAdd(&sm.bins[(int)((key >> shift) & 255u)], 1);
@@ -589,7 +504,8 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
 
   // ---- barrier of the request's CTAs
   __syncthreads();
-  if (tid == 0) sm.flag = request_barrier(w.tick + b, nch);
+  if (tid == 0) request_arrive(w.tick + b);
+  if (tid == 0) sm.flag = request_wait(w.tick + b, nch);
   __syncthreads();
   if (!sm.flag) {
     if (tid == 0) atomicCAS(w.err, 0, kErrTimeout);
@@ -783,7 +699,19 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
 
   const int n = min(__ldcg(w.cand_n + b), max_len);
   const bool staged = n <= kCandCap;
-  const uint64_t kstar = exact_threshold(cb, n, k - above, s_key, sm);
+  if (staged) {
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const int2 e = __ldcg(cb + i);
+      s_key[i] = order_key(e.x, e.y);
+    }
+    __syncthreads();
+  }
+  auto key_at = [&](int i) -> uint64_t {
+    if (staged) return s_key[i];
+    const int2 e = __ldcg(cb + i);
+    return order_key(e.x, e.y);
+  };
+  const uint64_t kstar = select_threshold(n, k - above, key_at, sm);
 
   if (len <= kBitmapTokens) {
     // ---- ordered output through the bitmap, staged in shared memory
