@@ -327,6 +327,30 @@ def main():
     value, total_s = job_throughput(sum(step_ms) / 1e3, args.steps, world, dist, dev)
     ms_per_step = total_s * 1e3 / args.steps
 
+    # ---- with an HBM slot table: the same step without the residency update
+    # (graph of the decode step alone), reported beside the full step
+    no_residency = None
+    if res is not None:
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=s):
+            step(s)
+        n2 = min(args.steps, 500)
+        st2 = [torch.cuda.Event(enable_timing=True) for _ in range(n2)]
+        en2 = [torch.cuda.Event(enable_timing=True) for _ in range(n2)]
+        with torch.cuda.stream(s):
+            for _ in range(args.warmup):
+                flush.zero_()
+                g2.replay()
+            for i in range(n2):
+                flush.zero_()
+                st2[i].record(s)
+                g2.replay()
+                en2[i].record(s)
+        torch.cuda.synchronize()
+        ms2 = statistics.median(a.elapsed_time(b) for a, b in zip(st2, en2))
+        no_residency = {"ms_per_step": ms2, "value": 1e3 / ms2, "steps": n2,
+                        "residency_update_ms": ms_per_step - ms2}
+
     # ---- per-stage times inside the real step (events between the stages)
     stage = {"scan": [], "topk": [], "attention": []}
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -382,6 +406,8 @@ def main():
             "stages_ms": stage_ms,
             "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
         }
+        if no_residency is not None:
+            line["without_residency_update"] = no_residency
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

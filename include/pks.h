@@ -145,9 +145,10 @@ typedef struct pks_decode_args {
   void* out;
   void* workspace;        /* device scratch owned by the caller, 256-byte aligned */
   size_t workspace_bytes;
-  int32_t attn_splits;    /* attention CTAs: 0 = one per resident slot on the GPU; else this
-                             many (1..1024), each taking an equal share of all selected
-                             (KV head group, request, position) work */
+  int32_t attn_splits;    /* attention CTAs: 0 = one per resident slot on the GPU, but no
+                             more than one per 32 selected positions; else this many
+                             (1..1024, at most one per position), each taking an equal share
+                             of all selected (KV head group, request, position) work */
   int32_t topk_mode;      /* 0 = one cooperative top-k launch when its grid fits on the GPU
                              at once, else two; 1 = always the two-kernel path */
   int32_t reserved[2];    /* must be 0 */

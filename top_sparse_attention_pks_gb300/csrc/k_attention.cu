@@ -90,6 +90,18 @@ struct SegCursor {
 
 __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
 
+// CTAs that take part for T positions: at most the grid and T, and with an
+// automatic grid (min_per_cta > 0) at most one per min_per_cta positions, so
+// that small steps are not cut into one-position pieces.
+__device__ __forceinline__ int64_t attn_effective_grid(int64_t T, int64_t grid, int min_per_cta) {
+  int64_t g = T < grid ? T : grid;
+  if (min_per_cta > 0) {
+    const int64_t cap = (T + min_per_cta - 1) / min_per_cta;
+    if (cap < g) g = cap;
+  }
+  return g < 1 ? 1 : g;
+}
+
 // CTA that owns flattened position f when [0, T) is cut into G equal ranges.
 __device__ __forceinline__ int owner_cta(int64_t f, int64_t T, int64_t G) {
   return (int)(((f + 1) * G + T - 1) / T - 1);
@@ -103,7 +115,8 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
                    int32_t* __restrict__ prefix_out, float2* __restrict__ part_ml,
                    float* __restrict__ part_o, __nv_bfloat16* __restrict__ out,
                    int32_t* __restrict__ err, int B, int Hq, int Hkv, int G, int page_size,
-                   int max_pages, int num_pages, int k, int trim, float scale_log2) {
+                   int max_pages, int num_pages, int k, int trim, int min_per_cta,
+                   float scale_log2) {
   constexpr int NT = HG * 32;
   constexpr int CH = D / 8;   // 16-byte chunks per head row
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
@@ -164,7 +177,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   // with fewer positions than CTAs only the first T CTAs take part, so every
   // participating CTA owns at least one position and the contributors of a
   // segment are exactly the CTAs from its first to its last owner
-  const int64_t GRID = T < (int64_t)gridDim.x ? T : (int64_t)gridDim.x;
+  const int64_t GRID = attn_effective_grid(T, gridDim.x, min_per_cta);
   const int cta = blockIdx.x;
 
   // requests with no position to visit (length 0) get zero outputs; CTA 0
@@ -430,7 +443,7 @@ template <int D>
 __global__ void __launch_bounds__(128)
 k_attention_merge(const int32_t* __restrict__ prefix, const float2* __restrict__ part_ml,
                   const float* __restrict__ part_o, __nv_bfloat16* __restrict__ out, int B,
-                  int Hq, int Hkv, int HG, int G, int attn_grid) {
+                  int Hq, int Hkv, int HG, int G, int attn_grid, int min_per_cta) {
   constexpr int DV4 = D / 4;  // float4 columns of a row (32 or 16)
   constexpr int kBatch = 16;  // contributors' o rows in flight per lane
   const float kNegInf = __int_as_float(0xff800000);
@@ -445,7 +458,7 @@ k_attention_merge(const int32_t* __restrict__ prefix, const float2* __restrict__
   const int p0 = prefix[b], p1 = prefix[b + 1];
   const int64_t T = Treq * (Hkv / HG);
   if (T == 0 || p1 == p0) return;
-  const int64_t GRID = T < (int64_t)attn_grid ? T : (int64_t)attn_grid;
+  const int64_t GRID = attn_effective_grid(T, attn_grid, min_per_cta);
   const int64_t seg_lo = (int64_t)g * Treq + p0;
   const int c_first = owner_cta(seg_lo, T, GRID), c_last = owner_cta(seg_lo + (p1 - p0) - 1, T, GRID);
   if (c_first == c_last) return;
@@ -542,6 +555,7 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
   int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * per_sm[dev & 63];
   if (grid > L.attn_grid_max) grid = L.attn_grid_max;
   const int G = a.Hq / a.Hkv;
+  const int min_per_cta = a.attn_splits > 0 ? 0 : kAttnMinPositions;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
   cudaError_t e = launch_ex(
       kern, dim3(grid), dim3(HG * 32), smem, s, /*pdl=*/true, /*coop=*/false, a.seq_lens,
@@ -550,13 +564,15 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
       (const int32_t*)a.topk_idx, reinterpret_cast<int32_t*>(ws + L.attn_prefix),
       reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
       reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.B, a.Hq,
-      a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, trim ? 1 : 0, scale_log2);
+      a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, trim ? 1 : 0, min_per_cta,
+      scale_log2);
   if (e != cudaSuccess) return e;
   return launch_ex(k_attention_merge<D>, dim3((a.Hq + 3) / 4, a.B), dim3(128), 0, s, true, false,
                    reinterpret_cast<const int32_t*>(ws + L.attn_prefix),
                    reinterpret_cast<const float2*>(ws + L.part_ml),
                    reinterpret_cast<const float*>(ws + L.part_o),
-                   reinterpret_cast<__nv_bfloat16*>(a.out), a.B, a.Hq, a.Hkv, (int)HG, G, grid);
+                   reinterpret_cast<__nv_bfloat16*>(a.out), a.B, a.Hq, a.Hkv, (int)HG, G, grid,
+                   min_per_cta);
 }
 
 // ---- allocation-free variant: scratch in a fixed device array -------------
@@ -610,6 +626,7 @@ cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cud
     return cudaSuccess;
   }
   const int G = a.Hq / a.Hkv;
+  const int min_per_cta = a.attn_splits > 0 ? 0 : kAttnMinPositions;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)a.D);
   kern<<<grid, HG * 32, smem, s>>>(
       a.seq_lens, a.block_table, reinterpret_cast<const __nv_bfloat16*>(a.q),
@@ -617,14 +634,15 @@ cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cud
       a.topk_idx, reinterpret_cast<int32_t*>(scratch + L.attn_prefix),
       reinterpret_cast<float2*>(scratch + L.part_ml), reinterpret_cast<float*>(scratch + L.part_o),
       reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(scratch + L.err), a.B,
-      a.Hq, a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, /*trim=*/0, scale_log2);
+      a.Hq, a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, /*trim=*/0, min_per_cta,
+      scale_log2);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_attention_merge<D><<<dim3((a.Hq + 3) / 4, a.B), 128, 0, s>>>(
       reinterpret_cast<const int32_t*>(scratch + L.attn_prefix),
       reinterpret_cast<const float2*>(scratch + L.part_ml),
       reinterpret_cast<const float*>(scratch + L.part_o), reinterpret_cast<__nv_bfloat16*>(a.out),
-      a.B, a.Hq, a.Hkv, HG, G, grid);
+      a.B, a.Hq, a.Hkv, HG, G, grid, min_per_cta);
   return cudaGetLastError();
 }
 

@@ -20,7 +20,8 @@
 //
 // k_residency_mark (one thread per selected position) marks pages of A in a
 // byte array; k_residency_update (one CTA of 1024 threads) does the rest with
-// block-wide scans and leaves its scratch arrays zero again.
+// block-wide scans over tiles read with 16-byte loads, and leaves its scratch
+// arrays zero again.
 
 #include "pks_internal.h"
 
@@ -79,6 +80,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_wa
   return (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
 }
 
+// Tiles of the three passes: a thread owns kPageTile consecutive pages,
+// kSlotTile consecutive LRU positions or slots, read with 16-byte loads and
+// gathered all at once, so that each tile costs about one round trip and one
+// block scan.
+constexpr int kPageTile = 32;
+constexpr int kSlotTile = 16;
+
 __global__ void __launch_bounds__(kUpdThreads)
 k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
                    int32_t* __restrict__ slot_page, int32_t* __restrict__ last_use,
@@ -104,40 +112,93 @@ k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
   if (!s_ok) return;
   const int step = s_step;
 
-  // ---- misses (ascending pages) and hits
-  const int pseg = (num_pages + kUpdThreads - 1) / kUpdThreads;
-  const int p_begin = min(num_pages, tid * pseg), p_end = min(num_pages, p_begin + pseg);
-  int cnt = 0;
-  for (int p = p_begin; p < p_end; ++p) cnt += (flag[p] && page_slot[p] < 0) ? 1 : 0;
-  // (page_slot entries are -1 or a slot below capacity in a valid state)
-  int n_miss;
-  int base = block_exclusive_scan(cnt, &n_miss, s_warp);
-  for (int p = p_begin; p < p_end; ++p) {
-    if (!flag[p]) continue;
-    const int s = page_slot[p];
-    if (s < 0) {
-      miss_list[base++] = p;
-    } else if (s < capacity) {
-      slot_flag[s] = 1;
-      last_use[s] = step;
+  // ---- misses (ascending pages) and hits; every page flag is cleared
+  int n_miss = 0;
+  for (int p0 = 0; p0 < num_pages; p0 += kPageTile * kUpdThreads) {
+    const int pb = p0 + tid * kPageTile;
+    uint32_t fl = 0;  // bit j: page pb + j is in A
+    int ps[kPageTile];
+    if (pb + kPageTile <= num_pages) {
+      const uint4* f4 = reinterpret_cast<const uint4*>(flag + pb);
+      const uint4 fa = f4[0], fb = f4[1];
+      const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+      for (int j = 0; j < kPageTile; ++j) fl |= (uint32_t)(((fw[j >> 2] >> (8 * (j & 3))) & 0xffu) != 0) << j;
+      const int4* s4 = reinterpret_cast<const int4*>(page_slot + pb);
+#pragma unroll
+      for (int q = 0; q < kPageTile / 4; ++q) {
+        const int4 v = s4[q];
+        ps[4 * q] = v.x;
+        ps[4 * q + 1] = v.y;
+        ps[4 * q + 2] = v.z;
+        ps[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPageTile; ++j) {
+        const bool in = pb + j < num_pages;
+        fl |= (uint32_t)(in && flag[pb + j] != 0) << j;
+        ps[j] = in ? page_slot[pb + j] : -1;
+      }
     }
-    flag[p] = 0;
+    uint32_t missm = 0;
+#pragma unroll
+    for (int j = 0; j < kPageTile; ++j) missm |= (uint32_t)(((fl >> j) & 1u) && ps[j] < 0) << j;
+    int tile_miss;
+    int base = n_miss + block_exclusive_scan(__popc(missm), &tile_miss, s_warp);
+#pragma unroll
+    for (int j = 0; j < kPageTile; ++j) {
+      if (!((fl >> j) & 1u)) continue;
+      const int sl = ps[j];
+      if (sl < 0) {
+        miss_list[base++] = pb + j;
+      } else if (sl < capacity) {
+        slot_flag[sl] = 1;
+        last_use[sl] = step;
+      }
+    }
+    if (fl) {
+      if (pb + kPageTile <= num_pages) {
+        uint4* f4 = reinterpret_cast<uint4*>(flag + pb);
+        f4[0] = make_uint4(0, 0, 0, 0);
+        f4[1] = make_uint4(0, 0, 0, 0);
+      } else {
+        for (int j = 0; j < kPageTile && pb + j < num_pages; ++j) flag[pb + j] = 0;
+      }
+    }
+    n_miss += tile_miss;
   }
-  __syncthreads();
+  __syncthreads();  // slot flags of the hits are visible to every thread
 
   // ---- victims: slots not hit this step, in LRU order
-  const int sseg = (capacity + kUpdThreads - 1) / kUpdThreads;
-  const int s_begin = min(capacity, tid * sseg), s_end = min(capacity, s_begin + sseg);
-  cnt = 0;
-  for (int i = s_begin; i < s_end; ++i) {
-    const int s = lru_order[i];
-    cnt += ((unsigned)s < (unsigned)capacity && !slot_flag[s]) ? 1 : 0;
-  }
-  int n_v;
-  base = block_exclusive_scan(cnt, &n_v, s_warp);
-  for (int i = s_begin; i < s_end; ++i) {
-    const int s = lru_order[i];
-    if ((unsigned)s < (unsigned)capacity && !slot_flag[s]) vict[base++] = s;
+  int n_v = 0;
+  for (int i0 = 0; i0 < capacity; i0 += kSlotTile * kUpdThreads) {
+    const int ib = i0 + tid * kSlotTile;
+    int sl[kSlotTile];
+    if (ib + kSlotTile <= capacity) {
+      const int4* l4 = reinterpret_cast<const int4*>(lru_order + ib);
+#pragma unroll
+      for (int q = 0; q < kSlotTile / 4; ++q) {
+        const int4 v = l4[q];
+        sl[4 * q] = v.x;
+        sl[4 * q + 1] = v.y;
+        sl[4 * q + 2] = v.z;
+        sl[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kSlotTile; ++j) sl[j] = ib + j < capacity ? lru_order[ib + j] : -1;
+    }
+    uint32_t vm = 0;  // bit j: slot sl[j] is a victim
+#pragma unroll
+    for (int j = 0; j < kSlotTile; ++j)
+      vm |= (uint32_t)((unsigned)sl[j] < (unsigned)capacity && !slot_flag[(unsigned)sl[j] < (unsigned)capacity ? sl[j] : 0]) << j;
+    int tile_v;
+    int base = n_v + block_exclusive_scan(__popc(vm), &tile_v, s_warp);
+#pragma unroll
+    for (int j = 0; j < kSlotTile; ++j)
+      if ((vm >> j) & 1u) vict[base++] = sl[j];
+    n_v += tile_v;
   }
   __syncthreads();
 
@@ -159,18 +220,35 @@ k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
   __syncthreads();
 
   // ---- new LRU order: untouched slots in their old order, then touched
-  // slots (last use = step) by slot number
+  // slots (last use = step) by slot number; every slot flag is cleared
   const int n_keep = n_v - n_admit;
   for (int i = tid; i < n_keep; i += kUpdThreads) lru_order[i] = vict[n_admit + i];
-  cnt = 0;
-  for (int s = s_begin; s < s_end; ++s) cnt += slot_flag[s] ? 1 : 0;
-  int n_touched;
-  base = n_keep + block_exclusive_scan(cnt, &n_touched, s_warp);
-  for (int s = s_begin; s < s_end; ++s) {
-    if (slot_flag[s]) {
-      lru_order[base++] = s;
-      slot_flag[s] = 0;
+  int n_touched = 0;
+  for (int s0 = 0; s0 < capacity; s0 += kSlotTile * kUpdThreads) {
+    const int sb = s0 + tid * kSlotTile;
+    uint32_t tm = 0;  // bit j: slot sb + j was touched
+    if (sb + kSlotTile <= capacity) {
+      const uint4 f = *reinterpret_cast<const uint4*>(slot_flag + sb);
+      const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int j = 0; j < kSlotTile; ++j) tm |= (uint32_t)(((fw[j >> 2] >> (8 * (j & 3))) & 0xffu) != 0) << j;
+    } else {
+#pragma unroll
+      for (int j = 0; j < kSlotTile; ++j) tm |= (uint32_t)(sb + j < capacity && slot_flag[sb + j] != 0) << j;
     }
+    int tile_t;
+    int base = n_keep + n_touched + block_exclusive_scan(__popc(tm), &tile_t, s_warp);
+#pragma unroll
+    for (int j = 0; j < kSlotTile; ++j)
+      if ((tm >> j) & 1u) lru_order[base++] = sb + j;
+    if (tm) {
+      if (sb + kSlotTile <= capacity) {
+        *reinterpret_cast<uint4*>(slot_flag + sb) = make_uint4(0, 0, 0, 0);
+      } else {
+        for (int j = 0; j < kSlotTile && sb + j < capacity; ++j) slot_flag[sb + j] = 0;
+      }
+    }
+    n_touched += tile_t;
   }
   if (tid == 0) {
     hdr[2] = step;

@@ -65,6 +65,9 @@ constexpr int kTopkCoopMaxChunks = 1024;
 // holds partials for.
 constexpr int kAttnTile = 16;
 constexpr int kAttnGridMax = 1024;
+// With an automatic grid, every attention CTA takes at least this many
+// selected positions (two tiles).
+constexpr int kAttnMinPositions = 2 * kAttnTile;
 
 // KV heads handled by one attention CTA (one warp each): the largest of
 // 8, 4, 2, 1 that divides Hkv.
