@@ -18,10 +18,12 @@
 // go to the back in slot order.  Both updates are order-preserving stream
 // compactions.
 //
-// k_residency_mark (one thread per selected position) marks pages of A in a
-// byte array; k_residency_update (one CTA of 1024 threads) does the rest with
-// block-wide scans over tiles read with 16-byte loads, and leaves its scratch
-// arrays zero again.
+// k_residency_mark (one thread per selected position, across the GPU) marks
+// the pages of A in a byte array and gives every hit its new last use and
+// slot flag (idempotent writes); k_residency_update (one CTA of 1024 threads)
+// does the ordered part — miss list, victims, admissions, the new LRU order —
+// as coalesced order-preserving compactions, and leaves its scratch arrays
+// zero again.
 
 #include "pks_internal.h"
 
@@ -35,24 +37,36 @@ __device__ __forceinline__ void flag_error(int32_t* err, int code) { atomicCAS(e
 
 __global__ void __launch_bounds__(kMarkThreads)
 k_residency_mark(const int32_t* __restrict__ topk, const int32_t* __restrict__ block_table,
-                 uint8_t* __restrict__ flag, int32_t* __restrict__ err, int B, int k,
-                 int page_size, int max_pages, int num_pages) {
+                 int32_t* __restrict__ hdr, const int32_t* __restrict__ page_slot,
+                 uint8_t* __restrict__ flag, uint8_t* __restrict__ slot_flag,
+                 int32_t* __restrict__ last_use, int B, int k, int page_size, int max_pages,
+                 int num_pages, int capacity) {
   const int64_t i = (int64_t)blockIdx.x * kMarkThreads + threadIdx.x;
   if (i >= (int64_t)B * k) return;
+  // a state buffer that pks_residency_init did not fill for these sizes is
+  // left untouched (the update kernel reports it)
+  if (hdr[5] != kResidencyMagic || hdr[0] != num_pages || hdr[1] != capacity) return;
   const int t = topk[i];
   if (t < 0) return;
   const int b = (int)(i / k);
   const int lp = t / page_size;
   if (lp >= max_pages) {
-    flag_error(err, kErrToken);
+    flag_error(hdr + 4, kErrToken);
     return;
   }
   const int page = block_table[(int64_t)b * max_pages + lp];
   if ((unsigned)page >= (unsigned)num_pages) {
-    flag_error(err, kErrPage);
+    flag_error(hdr + 4, kErrPage);
     return;
   }
   flag[page] = 1;
+  // a hit: the slot's last use becomes this step (the same values from every
+  // thread that selected a token of the page)
+  const int sl = page_slot[page];
+  if ((unsigned)sl < (unsigned)capacity) {
+    slot_flag[sl] = 1;
+    last_use[sl] = hdr[2] + 1;
+  }
 }
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_warp) {
@@ -80,12 +94,51 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_wa
   return (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
 }
 
-// Tiles of the three passes: a thread owns kPageTile consecutive pages,
-// kSlotTile consecutive LRU positions or slots, read with 16-byte loads and
-// gathered all at once, so that each tile costs about one round trip and one
-// block scan.
-constexpr int kPageTile = 32;
-constexpr int kSlotTile = 16;
+// Order-preserving compaction of n items in CTA-wide rounds of 32 per thread:
+// item (round r, thread t) is index base + r * 1024 + t, so every warp load
+// and store is coalesced.  keep(i) says whether item i is kept; emit(i, pos)
+// writes it at position pos of the output.  Warp ballots give the counts of
+// each (round, warp), one block scan over those 1024 counts gives every
+// warp's output offset.  Returns the number kept.
+template <typename Keep, typename Emit>
+__device__ __forceinline__ int compact(int n, int* s_cnt, int* s_warp, Keep keep, Emit emit) {
+  constexpr int kRounds = 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int kept = 0;
+  for (int base = 0; base < n; base += kRounds * kUpdThreads) {
+    uint32_t mine = 0;  // bit r: this thread's item of round r is kept
+    // keep() is evaluated on a clamped index so that every round's loads are
+    // unconditional and go out together
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int idx = base + r * kUpdThreads + tid;
+      const bool k = keep(idx < n ? idx : n - 1);
+      mine |= (uint32_t)(idx < n && k) << r;
+    }
+    // counts of (round, warp) in round-major order: entry r * 32 + warp
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const uint32_t m = __ballot_sync(0xffffffffu, (mine >> r) & 1u);
+      if (lane == 0) s_cnt[r * 32 + warp] = __popc(m);
+    }
+    __syncthreads();
+    int total;
+    const int v = s_cnt[tid];  // entry tid = (round tid / 32, warp tid % 32)
+    const int off = block_exclusive_scan(v, &total, s_warp);
+    s_cnt[tid] = off;
+    __syncthreads();
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 8
+    for (int r = 0; r < kRounds; ++r) {
+      const uint32_t m = __ballot_sync(0xffffffffu, (mine >> r) & 1u);
+      if ((mine >> r) & 1u)
+        emit(base + r * kUpdThreads + tid, kept + s_cnt[r * 32 + warp] + __popc(m & lt));
+    }
+    kept += total;
+    __syncthreads();  // s_cnt is reused by the next tile
+  }
+  return kept;
+}
 
 __global__ void __launch_bounds__(kUpdThreads)
 k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
@@ -95,6 +148,7 @@ k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
                    int32_t* __restrict__ miss_list, int32_t* __restrict__ n_miss_out,
                    int num_pages, int capacity) {
   __shared__ int s_warp[32];
+  __shared__ int s_cnt[kUpdThreads];
   __shared__ int s_step, s_new_resident, s_ok;
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -112,94 +166,26 @@ k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
   if (!s_ok) return;
   const int step = s_step;
 
-  // ---- misses (ascending pages) and hits; every page flag is cleared
-  int n_miss = 0;
-  for (int p0 = 0; p0 < num_pages; p0 += kPageTile * kUpdThreads) {
-    const int pb = p0 + tid * kPageTile;
-    uint32_t fl = 0;  // bit j: page pb + j is in A
-    int ps[kPageTile];
-    if (pb + kPageTile <= num_pages) {
-      const uint4* f4 = reinterpret_cast<const uint4*>(flag + pb);
-      const uint4 fa = f4[0], fb = f4[1];
-      const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-#pragma unroll
-      for (int j = 0; j < kPageTile; ++j) fl |= (uint32_t)(((fw[j >> 2] >> (8 * (j & 3))) & 0xffu) != 0) << j;
-      const int4* s4 = reinterpret_cast<const int4*>(page_slot + pb);
-#pragma unroll
-      for (int q = 0; q < kPageTile / 4; ++q) {
-        const int4 v = s4[q];
-        ps[4 * q] = v.x;
-        ps[4 * q + 1] = v.y;
-        ps[4 * q + 2] = v.z;
-        ps[4 * q + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kPageTile; ++j) {
-        const bool in = pb + j < num_pages;
-        fl |= (uint32_t)(in && flag[pb + j] != 0) << j;
-        ps[j] = in ? page_slot[pb + j] : -1;
-      }
-    }
-    uint32_t missm = 0;
-#pragma unroll
-    for (int j = 0; j < kPageTile; ++j) missm |= (uint32_t)(((fl >> j) & 1u) && ps[j] < 0) << j;
-    int tile_miss;
-    int base = n_miss + block_exclusive_scan(__popc(missm), &tile_miss, s_warp);
-#pragma unroll
-    for (int j = 0; j < kPageTile; ++j) {
-      if (!((fl >> j) & 1u)) continue;
-      const int sl = ps[j];
-      if (sl < 0) {
-        miss_list[base++] = pb + j;
-      } else if (sl < capacity) {
-        slot_flag[sl] = 1;
-        last_use[sl] = step;
-      }
-    }
-    if (fl) {
-      if (pb + kPageTile <= num_pages) {
-        uint4* f4 = reinterpret_cast<uint4*>(flag + pb);
-        f4[0] = make_uint4(0, 0, 0, 0);
-        f4[1] = make_uint4(0, 0, 0, 0);
-      } else {
-        for (int j = 0; j < kPageTile && pb + j < num_pages; ++j) flag[pb + j] = 0;
-      }
-    }
-    n_miss += tile_miss;
+  // ---- misses: pages of A without a slot, ascending (the mark kernel has
+  // already given the hits their new last use and slot flag)
+  const int n_miss = compact(
+      num_pages, s_cnt, s_warp, [&](int p) { return (flag[p] != 0) & (page_slot[p] < 0); },
+      [&](int p, int pos) { miss_list[pos] = p; });
+  // every page flag is cleared for the next step
+  for (int i = tid * 16; i < num_pages; i += kUpdThreads * 16) {
+    if (i + 16 <= num_pages) *reinterpret_cast<uint4*>(flag + i) = make_uint4(0, 0, 0, 0);
+    else for (int j = i; j < num_pages; ++j) flag[j] = 0;
   }
-  __syncthreads();  // slot flags of the hits are visible to every thread
 
   // ---- victims: slots not hit this step, in LRU order
-  int n_v = 0;
-  for (int i0 = 0; i0 < capacity; i0 += kSlotTile * kUpdThreads) {
-    const int ib = i0 + tid * kSlotTile;
-    int sl[kSlotTile];
-    if (ib + kSlotTile <= capacity) {
-      const int4* l4 = reinterpret_cast<const int4*>(lru_order + ib);
-#pragma unroll
-      for (int q = 0; q < kSlotTile / 4; ++q) {
-        const int4 v = l4[q];
-        sl[4 * q] = v.x;
-        sl[4 * q + 1] = v.y;
-        sl[4 * q + 2] = v.z;
-        sl[4 * q + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kSlotTile; ++j) sl[j] = ib + j < capacity ? lru_order[ib + j] : -1;
-    }
-    uint32_t vm = 0;  // bit j: slot sl[j] is a victim
-#pragma unroll
-    for (int j = 0; j < kSlotTile; ++j)
-      vm |= (uint32_t)((unsigned)sl[j] < (unsigned)capacity && !slot_flag[(unsigned)sl[j] < (unsigned)capacity ? sl[j] : 0]) << j;
-    int tile_v;
-    int base = n_v + block_exclusive_scan(__popc(vm), &tile_v, s_warp);
-#pragma unroll
-    for (int j = 0; j < kSlotTile; ++j)
-      if ((vm >> j) & 1u) vict[base++] = sl[j];
-    n_v += tile_v;
-  }
+  const int n_v = compact(
+      capacity, s_cnt, s_warp,
+      [&](int i) {
+        const int sl = lru_order[i];
+        const bool in = (unsigned)sl < (unsigned)capacity;
+        return in & (slot_flag[in ? sl : 0] == 0);
+      },
+      [&](int i, int pos) { vict[pos] = lru_order[i]; });
   __syncthreads();
 
   // ---- admission: i-th miss -> i-th victim
@@ -223,32 +209,13 @@ k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
   // slots (last use = step) by slot number; every slot flag is cleared
   const int n_keep = n_v - n_admit;
   for (int i = tid; i < n_keep; i += kUpdThreads) lru_order[i] = vict[n_admit + i];
-  int n_touched = 0;
-  for (int s0 = 0; s0 < capacity; s0 += kSlotTile * kUpdThreads) {
-    const int sb = s0 + tid * kSlotTile;
-    uint32_t tm = 0;  // bit j: slot sb + j was touched
-    if (sb + kSlotTile <= capacity) {
-      const uint4 f = *reinterpret_cast<const uint4*>(slot_flag + sb);
-      const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-      for (int j = 0; j < kSlotTile; ++j) tm |= (uint32_t)(((fw[j >> 2] >> (8 * (j & 3))) & 0xffu) != 0) << j;
-    } else {
-#pragma unroll
-      for (int j = 0; j < kSlotTile; ++j) tm |= (uint32_t)(sb + j < capacity && slot_flag[sb + j] != 0) << j;
-    }
-    int tile_t;
-    int base = n_keep + n_touched + block_exclusive_scan(__popc(tm), &tile_t, s_warp);
-#pragma unroll
-    for (int j = 0; j < kSlotTile; ++j)
-      if ((tm >> j) & 1u) lru_order[base++] = sb + j;
-    if (tm) {
-      if (sb + kSlotTile <= capacity) {
-        *reinterpret_cast<uint4*>(slot_flag + sb) = make_uint4(0, 0, 0, 0);
-      } else {
-        for (int j = 0; j < kSlotTile && sb + j < capacity; ++j) slot_flag[sb + j] = 0;
-      }
-    }
-    n_touched += tile_t;
+  compact(
+      capacity, s_cnt, s_warp, [&](int sl) { return slot_flag[sl] != 0; },
+      [&](int sl, int pos) { lru_order[n_keep + pos] = sl; });
+  __syncthreads();
+  for (int i = tid * 16; i < capacity; i += kUpdThreads * 16) {
+    if (i + 16 <= capacity) *reinterpret_cast<uint4*>(slot_flag + i) = make_uint4(0, 0, 0, 0);
+    else for (int j = i; j < capacity; ++j) slot_flag[j] = 0;
   }
   if (tid == 0) {
     hdr[2] = step;
@@ -271,9 +238,10 @@ cudaError_t launch_residency(int32_t* state, int32_t num_pages, int32_t capacity
   const int64_t n = (int64_t)B * k;
   if (n > 0) {
     const int64_t grid = (n + kMarkThreads - 1) / kMarkThreads;
-    k_residency_mark<<<(unsigned)grid, kMarkThreads, 0, s>>>(topk_idx, block_table, flag,
-                                                             state + 4, B, k, page_size,
-                                                             max_pages, num_pages);
+    k_residency_mark<<<(unsigned)grid, kMarkThreads, 0, s>>>(
+        topk_idx, block_table, state, reinterpret_cast<const int32_t*>(base + off_page_slot), flag,
+        base + off_slot_flag, reinterpret_cast<int32_t*>(base + off_last_use), B, k, page_size,
+        max_pages, num_pages, capacity);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
