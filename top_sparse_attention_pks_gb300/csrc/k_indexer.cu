@@ -7,24 +7,20 @@
 // notes that selection needs the whole context resident in HBM: this kernel
 // streams every indexer key once and is bound by HBM bandwidth.
 //
-// Work split: the tokens of all requests are cut into CTA rounds of one
-// request; a persistent grid (one CTA per SM) gives each CTA a contiguous
-// range of rounds.  Keys stream from HBM straight into registers with
-// coalesced 16-byte loads (no shared-memory staging: on GB300 register
-// loads with 16+ warps an SM reach a higher read bandwidth than cp.async or
-// TMA fills of shared memory), one round ahead.  Two kernels:
-//  * 4 or 8 indexer heads: the head dot products are int8 tensor-core MMAs
-//    (k_indexer_scan_mma, 32 warps an SM);
-//  * 1 or 2 heads: dp4a with a transposed butterfly across the lanes of a
-//    token (k_indexer_scan_reg, 16 warps an SM).
-// Each score is binned into the request's shared-memory histogram, which is
-// added to the global one at the end (it seeds the top-k selection).
+// Work split: the tokens of all requests are cut into CTA rounds of 1024
+// tokens of one request; a persistent grid (one 1024-thread CTA per SM) gives
+// each CTA a contiguous range of rounds.  Keys stream from HBM straight into
+// registers with coalesced 16-byte loads (no shared-memory staging: on GB300
+// register loads with 32 warps an SM reach a higher read bandwidth than
+// cp.async or TMA fills of shared memory); the head dot products are int8
+// tensor-core MMAs for any number of heads up to 8.  Each score is binned into
+// the request's shared-memory histogram, which is added to the global one when
+// the CTA leaves the request (it seeds the top-k selection).
 
 #include "pks_internal.h"
 
 namespace pks {
 namespace {
-
 
 __device__ __forceinline__ int score_bin(int s) {
   if (s == 0) return kScoreBins / 2;
@@ -77,233 +73,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_wa
 }
 
 // ---------------------------------------------------------------------------
-// Register-streaming variant.  Keys go from HBM straight into registers with
-// coalesced 16-byte loads (each warp-wide load covers Di/16 lanes x 32/(Di/16)
-// tokens = 512 contiguous bytes), double-buffered one round ahead, 16 warps
-// per SM.  Lane (g, j) holds chunk j of the tokens j' * (32 / (Di/16)) + g of
-// its round and multiplies it with chunk j of every indexer head (query
-// chunks live in registers).  A transposed butterfly across the Di/16 lanes of
-// a token then halves the token slots at each step, so that after log2(Di/16)
-// steps lane (g, j) holds the full head dot products of token j*(32/(Di/16))+g
-// and finishes its score alone.  Shared memory holds only the histogram and
-// the round prefix; the loop has no block-wide barrier.
-
-constexpr int kRegWarps = 16;
-constexpr int kRegThreads = kRegWarps * 32;
-constexpr int kRegRound = kRegThreads;  // tokens per CTA round (32 per warp)
-
-template <int HI, int DI>
-__global__ void __launch_bounds__(kRegThreads, 1)
-k_indexer_scan_reg(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
-                   const int8_t* __restrict__ q_idx, const int32_t* __restrict__ w_idx,
-                   const int8_t* __restrict__ idx_k, int32_t* __restrict__ scores, int64_t ld,
-                   int32_t* __restrict__ hist, int32_t* __restrict__ err, int B, int max_pages,
-                   int page_size, int page_shift, int num_pages, int k) {
-  constexpr int LPT = DI / 16;  // lanes per token (one 16-byte chunk each)
-  constexpr int TPI = 32 / LPT;  // tokens per warp-wide load
-  constexpr int NI = LPT;        // loads per lane per round (32 tokens)
-
-  extern __shared__ int smem_i[];
-  // the top-k grid may take SM slots as soon as this grid's CTAs retire
-  pdl_launch_dependents();
-  int* s_hist = smem_i;                 // [kScoreBins]
-  int* s_prefix = smem_i + kScoreBins;  // [B + 1]
-  __shared__ int s_warp[kRegThreads / 32];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane / LPT, j = lane % LPT;
-  const int max_len = max_pages * page_size;
-
-  // rounds per request -> exclusive prefix in shared memory
-  const int per = (B + kRegThreads - 1) / kRegThreads;
-  int local = 0;
-  for (int i = 0; i < per; ++i) {
-    const int b = tid * per + i;
-    if (b < B) {
-      int len = seq_lens[b];
-      if (len < 0 || len > max_len) {
-        if (blockIdx.x == 0) flag_error(err, kErrLen);
-        len = 0;
-      }
-      local += (len + kRegRound - 1) / kRegRound;
-    }
-  }
-  int total_rounds;
-  int run = block_exclusive_scan<kRegThreads>(local, &total_rounds, s_warp);
-  for (int i = 0; i < per; ++i) {
-    const int b = tid * per + i;
-    if (b < B) {
-      s_prefix[b] = run;
-      int len = seq_lens[b];
-      if (len < 0 || len > max_len) len = 0;
-      run += (len + kRegRound - 1) / kRegRound;
-    }
-  }
-  if (tid == 0) s_prefix[B] = total_rounds;
-  for (int i = tid; i < kScoreBins; i += kRegThreads) s_hist[i] = 0;
-  __syncthreads();
-
-  const int64_t G = gridDim.x;
-  const int begin = (int)((int64_t)blockIdx.x * total_rounds / G);
-  const int end = (int)((int64_t)(blockIdx.x + 1) * total_rounds / G);
-  if (begin >= end) return;
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_prefix[mid] <= begin) lo = mid; else hi = mid - 1;
-  }
-
-  // ---- page lookups, one token per lane, issued two rounds ahead
-  int lk_b = lo, lk_len = 0, lk_next = s_prefix[lo + 1];
-  {
-    const int len = seq_lens[lk_b];
-    lk_len = (len < 0 || len > max_len) ? 0 : len;
-  }
-  // -> physical key row of this lane's token of round `item` (page id still
-  // to be checked), or -1; `slot` receives the row within the page
-  auto lookup = [&](int item, int& slot) -> int {
-    while (lk_next <= item) {
-      ++lk_b;
-      lk_next = s_prefix[lk_b + 1];
-      const int len = seq_lens[lk_b];
-      lk_len = (len < 0 || len > max_len) ? 0 : len;
-    }
-    const int t = (item - s_prefix[lk_b]) * kRegRound + warp * 32 + lane;
-    slot = -1;
-    if (t >= lk_len) return -1;
-    const int lp = page_shift >= 0 ? (t >> page_shift) : t / page_size;
-    slot = page_shift >= 0 ? (t & (page_size - 1)) : t % page_size;
-    return __ldg(block_table + (int64_t)lk_b * max_pages + lp);
-  };
-  auto to_row = [&](int page, int slot) -> int {
-    if (slot < 0) return -1;
-    if ((unsigned)page < (unsigned)num_pages) return page * page_size + slot;
-    flag_error(err, kErrPage);
-    return -1;
-  };
-  auto load_round = [&](int row, int4 (&buf)[NI]) {
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int rr = __shfl_sync(0xffffffffu, row, i * TPI + g);
-      buf[i] = rr >= 0 ? __ldcs(reinterpret_cast<const int4*>(idx_k + (int64_t)rr * DI) + j)
-                       : make_int4(0, 0, 0, 0);
-    }
-  };
-
-  int4 cur[NI], nxt[NI];
-  int pg1, sl1, pg2, sl2;  // lookups of rounds item+1 and item+2
-  {
-    int sl0;
-    const int pg0 = lookup(begin, sl0);
-    load_round(to_row(pg0, sl0), cur);
-    pg1 = begin + 1 < end ? lookup(begin + 1, sl1) : (sl1 = -1, -1);
-    pg2 = begin + 2 < end ? lookup(begin + 2, sl2) : (sl2 = -1, -1);
-  }
-
-  int4 qv[HI];
-  int w[HI];
-  int cb = -1, cb_len = 0, cb_first = 0, cb_next = 0;
-  bool do_hist = false;
-  for (int item = begin; item < end; ++item) {
-    if (item + 1 < end) load_round(to_row(pg1, sl1), nxt);
-    {
-      int sl3 = -1;
-      const int pg3 = item + 3 < end ? lookup(item + 3, sl3) : -1;
-      pg1 = pg2;
-      sl1 = sl2;
-      pg2 = pg3;
-      sl2 = sl3;
-    }
-    if (item >= cb_next) {
-      // request switch (uniform across the CTA): flush the histogram, load q
-      int b = cb < 0 ? lo : cb;
-      while (s_prefix[b + 1] <= item) ++b;
-      if (do_hist) {
-        __syncthreads();
-        int32_t* gh = hist + (int64_t)cb * kScoreBins;
-        for (int i = tid; i < kScoreBins; i += kRegThreads) {
-          const int cnt = s_hist[i];
-          if (cnt) {
-            atomicAdd(gh + i, cnt);
-            s_hist[i] = 0;
-          }
-        }
-      }
-      __syncthreads();
-      cb = b;
-      cb_first = s_prefix[b];
-      cb_next = s_prefix[b + 1];
-      const int len = seq_lens[b];
-      cb_len = (len < 0 || len > max_len) ? 0 : len;
-      do_hist = hist != nullptr && cb_len > k;
-#pragma unroll
-      for (int h = 0; h < HI; ++h) {
-        qv[h] = __ldg(reinterpret_cast<const int4*>(q_idx + ((int64_t)b * HI + h) * DI) + j);
-        w[h] = __ldg(w_idx + h);
-      }
-    }
-
-    // partial dot products: p[i][h] over this lane's chunk of token slot i
-    int p[NI][HI];
-#pragma unroll
-    for (int i = 0; i < NI; ++i)
-#pragma unroll
-      for (int h = 0; h < HI; ++h) {
-        int a = __dp4a(cur[i].x, qv[h].x, 0);
-        a = __dp4a(cur[i].y, qv[h].y, a);
-        a = __dp4a(cur[i].z, qv[h].z, a);
-        p[i][h] = __dp4a(cur[i].w, qv[h].w, a);
-      }
-    // transposed butterfly: at stride s the lane keeps the upper half of its
-    // slots when (j & s) is set, and adds its partner's copy of them
-#pragma unroll
-    for (int s = LPT / 2, n = NI; s >= 1; s >>= 1, n >>= 1) {
-      const bool up = (j & s) != 0;
-#pragma unroll
-      for (int m = 0; m < n / 2; ++m)
-#pragma unroll
-        for (int h = 0; h < HI; ++h) {
-          const int keep = up ? p[m + n / 2][h] : p[m][h];
-          const int send = up ? p[m][h] : p[m + n / 2][h];
-          p[m][h] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-    }
-    int score = 0;
-#pragma unroll
-    for (int h = 0; h < HI; ++h) score += w[h] * max(p[0][h], 0);
-
-    // lane (g, j) now holds token slot j, i.e. token j * TPI + g of the round
-    const int t = (item - cb_first) * kRegRound + warp * 32 + j * TPI + g;
-    const bool valid = t < cb_len;
-    if (valid) store_score_keep(scores + (int64_t)cb * ld + t, score);
-    if (do_hist) {
-      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-      if (valid) {
-        const int bin = score_bin(score);
-        const unsigned peers = __match_any_sync(vmask, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < NI; ++i) cur[i] = nxt[i];
-  }
-  if (do_hist) {
-    __syncthreads();
-    int32_t* gh = hist + (int64_t)cb * kScoreBins;
-    for (int i = tid; i < kScoreBins; i += kRegThreads) {
-      const int cnt = s_hist[i];
-      if (cnt) atomicAdd(gh + i, cnt);
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Tensor-core variant for 4 or 8 indexer heads.  The head dot products of 16
-// tokens are one int8 MMA tile per 32 key bytes: m16n8k32 with the tokens as
-// M, the (zero-padded to 8) heads as N and the key bytes as K, int32
-// accumulate - exact, like dp4a, but the cross-lane sum happens inside the
-// tensor core, so a 32-token round costs 8 MMAs instead of ~100 dp4a and
-// shuffles per lane.  Keys stream from HBM straight into the A fragments: lane
+// The head dot products of 16 tokens are one int8 MMA tile per 32 key bytes:
+// m16n8k32 with the tokens as M, the (zero-padded to 8) heads as N and the key
+// bytes as K, int32 accumulate - exact, like dp4a, but the cross-lane sum
+// happens inside the tensor core, so a 32-token round costs 8 MMAs instead of
+// ~100 dp4a and shuffles per lane, whatever the number of heads.  Keys stream
+// from HBM straight into the A fragments: lane
 // (g, t) loads bytes [16t, 16t+16) and [64+16t, 64+16t+16) of tokens g and
 // g+8 of each 16-token tile (each warp-wide load reads 8 rows x 64 contiguous
 // bytes); the K order inside a tile is permuted identically in the key and
@@ -319,7 +94,7 @@ __device__ __forceinline__ void imma_16832(int (&c)[4], int a0, int a1, int a2, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int HI, int DI, int NT, bool DB>
+template <int HI, int DI, int NT>
 __global__ void __launch_bounds__(NT, 1)
 k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                    const int8_t* __restrict__ q_idx, const int32_t* __restrict__ w_idx,
@@ -509,25 +284,12 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     if (do_hist && valid) atomicAdd(&s_hist[score_bin(score)], 1);
   };
 
-  if constexpr (DB) {
-    // ping-pong: round i+1 loads into one buffer while round i computes from
-    // the other, and round i+2's loads go out before round i+1 is awaited
-    int4 ba[NLD], bb[NLD];
-    load_round(next_row(), ba);
-    for (int item = begin; item < end; item += 2) {
-      if (item + 1 < end) load_round(next_row(), bb);
-      process(item, ba);
-      if (item + 1 >= end) break;
-      if (item + 2 < end) load_round(next_row(), ba);
-      process(item + 1, bb);
-    }
-  } else {
-    // single-buffered: the other warps of the SM overlap a warp's load latency
-    int4 cur[NLD];
-    for (int item = begin; item < end; ++item) {
-      load_round(next_row(), cur);
-      process(item, cur);
-    }
+  // single-buffered: the other warps of the SM overlap a warp's load latency
+  // (double-buffering the key registers measured slower on GB300)
+  int4 cur[NLD];
+  for (int item = begin; item < end; ++item) {
+    load_round(next_row(), cur);
+    process(item, cur);
   }
   if (do_hist) {
     __syncthreads();
@@ -553,9 +315,8 @@ cudaError_t raise_smem(K kern, size_t smem, size_t (&configured)[64]) {
   return cudaSuccess;
 }
 
-// int8-MMA scan: threads a CTA (one CTA an SM) and double buffering
+// threads a CTA (one CTA an SM)
 constexpr int kMmaThreads = 1024;
-constexpr bool kMmaDoubleBuffer = false;
 
 template <int HI, int DI>
 cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld, int32_t* hist,
@@ -576,11 +337,7 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
                                                   a.k);
     return cudaGetLastError();
   };
-  // 4 or 8 heads: int8 MMA; 1 or 2 heads: dp4a
-  if constexpr (HI >= 4)
-    return go(k_indexer_scan_mma<HI, DI, kMmaThreads, kMmaDoubleBuffer>, kMmaThreads);
-  else
-    return go(k_indexer_scan_reg<HI, DI>, kRegThreads);
+  return go(k_indexer_scan_mma<HI, DI, kMmaThreads>, kMmaThreads);
 }
 
 }  // namespace
