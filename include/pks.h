@@ -171,6 +171,11 @@ pks_status pks_decode_workspace_init(const pks_decode_args* args, pks_stream str
  * re-initialised. */
 pks_status pks_decode_step(const pks_decode_args* args, pks_stream stream);
 
+/* Stages 1 and 2 alone (scan and top-k, writing args->topk_idx), for callers
+ * that route attention elsewhere, e.g. through a residency table
+ * (pks_sparse_attention_resident).  q, kv_k, kv_v and out are not used. */
+pks_status pks_decode_select(const pks_decode_args* args, pks_stream stream);
+
 /* Kernels one pks_decode_step with these shapes enqueues on the current
  * device (host only; pointers may be NULL).  INVALID: bad shapes or out NULL. */
 pks_status pks_decode_launches(const pks_decode_args* args, int32_t* launches);
@@ -263,6 +268,37 @@ pks_status pks_residency_update(void* state, int32_t num_pages, int32_t capacity
                                 int32_t k, int32_t page_size, int32_t max_pages,
                                 const int32_t* topk_idx, const int32_t* block_table,
                                 int32_t* miss_list, int32_t* n_miss, pks_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Miss fetch and attention through the residency table ([SA] HiSparse
+ * paragraph: the KV cache lives in host DRAM, HBM holds an LRU cache of it,
+ * a top-k miss is loaded into HBM).  The pages' K/V pools (host_k, host_v:
+ * [num_pages, page_size, Hkv, D] bf16) live in device-accessible host memory
+ * (pinned, read over the CPU-GPU link); the HBM slot pools (slot_k, slot_v:
+ * [capacity, page_size, Hkv, D] bf16) hold the resident pages, slot s holding
+ * page slot_page[s].  A step: pks_decode_select, pks_residency_update,
+ * pks_residency_fetch, pks_sparse_attention_resident.
+ * ---------------------------------------------------------------------- */
+
+/* Copy the misses of the last pks_residency_update that were admitted (a
+ * page of miss_list[0..*n_miss) that now has a slot) from the host pools into
+ * their slots: page_bytes = page_size * Hkv * D * 2 bytes of K and of V per
+ * page.  Misses that were not admitted are skipped (the attention reads them
+ * from the host pools).  All pointers 16-byte aligned; page_bytes a multiple
+ * of 16 (INVALID otherwise).  One kernel launch. */
+pks_status pks_residency_fetch(const void* state, int32_t num_pages, int32_t capacity,
+                               const int32_t* miss_list, const int32_t* n_miss,
+                               const void* host_k, const void* host_v, void* slot_k,
+                               void* slot_v, int64_t page_bytes, pks_stream stream);
+
+/* pks_sparse_attention with K/V found through the residency table: args->kv_k
+ * and args->kv_v are the host pools (args->num_pages pages); a token of a
+ * resident page is read from its slot in slot_k / slot_v, any other from the
+ * host pools.  Same grid, arithmetic and result as pks_sparse_attention on
+ * the host pools.  Uses the workspace; state as for pks_residency_update. */
+pks_status pks_sparse_attention_resident(const pks_decode_args* args, const void* state,
+                                         int32_t capacity, const void* slot_k,
+                                         const void* slot_v, pks_stream stream);
 
 #ifdef __cplusplus
 }

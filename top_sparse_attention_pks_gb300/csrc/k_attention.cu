@@ -116,7 +116,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
                    float* __restrict__ part_o, __nv_bfloat16* __restrict__ out,
                    int32_t* __restrict__ err, int B, int Hq, int Hkv, int G, int page_size,
                    int max_pages, int num_pages, int k, int trim, int min_per_cta,
-                   float scale_log2) {
+                   float scale_log2, ResidentKv rk) {
   constexpr int NT = HG * 32;
   constexpr int CH = D / 8;   // 16-byte chunks per head row
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
@@ -290,7 +290,16 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
             flag_error(err, kErrToken);
           } else {
             const int page = block_table[(int64_t)c.b * max_pages + t / page_size];
-            if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
+            if ((unsigned)page < (unsigned)num_pages) {
+              row = page * page_size + t % page_size;
+              if (rk.page_slot != nullptr) {
+                // resident page: its slot's row; otherwise the host pool's
+                // row, encoded as -(row) - 2 (-1 stays "no token")
+                const int sl = rk.page_slot[page];
+                row = (unsigned)sl < (unsigned)rk.capacity ? sl * page_size + t % page_size
+                                                           : -row - 2;
+              }
+            }
             else flag_error(err, kErrPage);
           }
         }
@@ -318,10 +327,14 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
         const int hh = rem / CH, c = rem % CH;
         const int row = r < n ? s_row[rbase + r] : -1;
         const int off = (r * HG + hh) * D + ((c ^ (r & 7)) << 3);
-        const int64_t src = row >= 0 ? ((int64_t)row * Hkv + g * HG + hh) * D + c * 8 : 0;
-        const int bytes = row >= 0 ? 16 : 0;  // 0 bytes: zero fill
-        cp_async16(smem_u32(sk + off), kv_k + src, bytes);
-        cp_async16(smem_u32(sv + off), kv_v + src, bytes);
+        // row >= 0: kv_k / kv_v (the pool, or the resident slots); row <= -2:
+        // the host pool's row -row - 2; -1: no token (zero fill)
+        const bool host = row < -1;
+        const int64_t prow = host ? -(int64_t)row - 2 : (int64_t)row;
+        const int64_t src = row != -1 ? (prow * Hkv + g * HG + hh) * D + c * 8 : 0;
+        const int bytes = row != -1 ? 16 : 0;  // 0 bytes: zero fill
+        cp_async16(smem_u32(sk + off), (host ? rk.host_k : kv_k) + src, bytes);
+        cp_async16(smem_u32(sv + off), (host ? rk.host_v : kv_v) + src, bytes);
       }
       ld_pos += n;
     };
@@ -376,7 +389,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int r = nt * 8 + cq + e;
-          const bool valid = r < n && s_row[rbase + r] >= 0;
+          const bool valid = r < n && s_row[rbase + r] != -1;
           x[nt][e] = valid ? sacc[nt][e] * scale_log2 : kNegInf;
           x[nt][e + 2] = valid ? sacc[nt][e + 2] * scale_log2 : kNegInf;
         }
@@ -533,7 +546,7 @@ size_t attn_smem_bytes(int B) {
 
 template <int D, int HG>
 cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
-                          bool trim, cudaStream_t s) {
+                          bool trim, const ResidentKv& rk, cudaStream_t s) {
   auto kern = k_sparse_attention<D, HG>;
   const size_t smem = attn_smem_bytes<D, HG>(a.B);
   // raise the dynamic shared-memory limit once per device and size (not a
@@ -565,7 +578,7 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
       reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
       reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.B, a.Hq,
       a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, trim ? 1 : 0, min_per_cta,
-      scale_log2);
+      scale_log2, rk);
   if (e != cudaSuccess) return e;
   return launch_ex(k_attention_merge<D>, dim3((a.Hq + 3) / 4, a.B), dim3(128), 0, s, true, false,
                    reinterpret_cast<const int32_t*>(ws + L.attn_prefix),
@@ -635,7 +648,7 @@ cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cud
       reinterpret_cast<float2*>(scratch + L.part_ml), reinterpret_cast<float*>(scratch + L.part_o),
       reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(scratch + L.err), a.B,
       a.Hq, a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, /*trim=*/0, min_per_cta,
-      scale_log2);
+      scale_log2, ResidentKv{});
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_attention_merge<D><<<dim3((a.Hq + 3) / 4, a.B), 128, 0, s>>>(
@@ -649,10 +662,10 @@ cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cud
 }  // namespace
 
 cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
-                             bool trim, cudaStream_t s) {
+                             bool trim, cudaStream_t s, const ResidentKv& rk) {
   const int hg = attn_heads_per_cta(a.Hkv);
 #define PKS_ATTN_CASE(D_, HG_) \
-  if (a.D == D_ && hg == HG_) return launch_attn_t<D_, HG_>(a, L, ws, trim, s);
+  if (a.D == D_ && hg == HG_) return launch_attn_t<D_, HG_>(a, L, ws, trim, rk, s);
   PKS_ATTN_CASE(64, 1)
   PKS_ATTN_CASE(64, 2)
   PKS_ATTN_CASE(64, 4)

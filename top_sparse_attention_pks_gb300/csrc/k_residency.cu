@@ -224,7 +224,65 @@ k_residency_update(int32_t* __restrict__ hdr, int32_t* __restrict__ page_slot,
   }
 }
 
+// Miss fetch ([SA] HiSparse paragraph: a top-k miss is loaded into HBM).
+// One CTA per admitted miss page at a time (grid-stride over the miss list):
+// the page's K and V bytes are read from the host pools (device-accessible
+// host memory, over the CPU-GPU link) with 16-byte loads, eight in flight per
+// thread, and written to the page's slot in the HBM slot pools.
+constexpr int kFetchThreads = 256;
+
+__global__ void __launch_bounds__(kFetchThreads)
+k_residency_fetch(const int32_t* __restrict__ page_slot, const int32_t* __restrict__ miss_list,
+                  const int32_t* __restrict__ n_miss, const int4* __restrict__ host_k,
+                  const int4* __restrict__ host_v, int4* __restrict__ slot_k,
+                  int4* __restrict__ slot_v, int64_t page_vec, int num_pages, int capacity) {
+  const int n = min(*n_miss, num_pages);
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const int p = miss_list[i];
+    if ((unsigned)p >= (unsigned)num_pages) continue;
+    const int sl = page_slot[p];
+    if ((unsigned)sl >= (unsigned)capacity) continue;  // reported, not admitted
+    const int4* sk = host_k + (int64_t)p * page_vec;
+    const int4* sv = host_v + (int64_t)p * page_vec;
+    int4* dk = slot_k + (int64_t)sl * page_vec;
+    int4* dv = slot_v + (int64_t)sl * page_vec;
+    constexpr int U = 4;
+    for (int64_t j0 = threadIdx.x; j0 < page_vec; j0 += (int64_t)kFetchThreads * U) {
+      int4 a[U], b[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = j0 + (int64_t)u * kFetchThreads;
+        if (j < page_vec) {
+          a[u] = __ldcs(sk + j);
+          b[u] = __ldcs(sv + j);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = j0 + (int64_t)u * kFetchThreads;
+        if (j < page_vec) {
+          dk[j] = a[u];
+          dv[j] = b[u];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_residency_fetch(const int32_t* page_slot, const int32_t* miss_list,
+                                   const int32_t* n_miss, const uint8_t* host_k,
+                                   const uint8_t* host_v, uint8_t* slot_k, uint8_t* slot_v,
+                                   int64_t page_bytes, int num_pages, int capacity,
+                                   cudaStream_t s) {
+  const int grid = device_sm_count() * 4;
+  k_residency_fetch<<<grid, kFetchThreads, 0, s>>>(
+      page_slot, miss_list, n_miss, reinterpret_cast<const int4*>(host_k),
+      reinterpret_cast<const int4*>(host_v), reinterpret_cast<int4*>(slot_k),
+      reinterpret_cast<int4*>(slot_v), page_bytes / 16, num_pages, capacity);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_residency(int32_t* state, int32_t num_pages, int32_t capacity, int32_t B,
                              int32_t k, int32_t page_size, int32_t max_pages,

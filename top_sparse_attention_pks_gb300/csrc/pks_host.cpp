@@ -310,12 +310,13 @@ pks_status pks_decode_workspace_init(const pks_decode_args* args, pks_stream str
 }
 
 static pks_status decode_impl(const pks_decode_args* args, pks_stream stream,
-                              pks_event const* ev) {
+                              pks_event const* ev, bool attention = true) {
   pks_status st = pks::check_shapes(args);
   if (st != PKS_OK) return st;
   if ((st = pks::check_common_ptrs(args)) != PKS_OK) return st;
   if ((st = pks::check_scan_ptrs(args)) != PKS_OK) return st;
-  if ((st = pks::check_attn_ptrs(args)) != PKS_OK) return st;
+  if (!args->topk_idx) return PKS_ERR_INVALID;
+  if (attention && (st = pks::check_attn_ptrs(args)) != PKS_OK) return st;
   const WorkspaceLayout L = pks::workspace_layout(*args);
   if ((st = pks::check_workspace(args, L)) != PKS_OK) return st;
   if (args->B == 0) return PKS_OK;
@@ -333,9 +334,13 @@ static pks_status decode_impl(const pks_decode_args* args, pks_stream stream,
   if (e == cudaSuccess) e = rec(1);
   if (e == cudaSuccess) e = pks::launch_topk(*args, L, ws, s);
   if (e == cudaSuccess) e = rec(2);
-  if (e == cudaSuccess) e = pks::launch_attention(*args, L, ws, /*trim=*/true, s);
+  if (attention && e == cudaSuccess) e = pks::launch_attention(*args, L, ws, /*trim=*/true, s);
   if (e == cudaSuccess) e = rec(3);
   return pks::from_cuda(e);
+}
+
+pks_status pks_decode_select(const pks_decode_args* args, pks_stream stream) {
+  return decode_impl(args, stream, nullptr, /*attention=*/false);
 }
 
 pks_status pks_decode_step(const pks_decode_args* args, pks_stream stream) {
@@ -530,6 +535,55 @@ pks_status pks_residency_update(void* state, int32_t num_pages, int32_t capacity
       static_cast<int32_t*>(state), num_pages, capacity, B, k, page_size, max_pages, topk_idx,
       block_table, miss_list, n_miss, R.page_slot, R.slot_page, R.last_use, R.lru_order, R.flag,
       R.slot_flag, R.vict, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pks_status pks_sparse_attention_resident(const pks_decode_args* args, const void* state,
+                                         int32_t capacity, const void* slot_k,
+                                         const void* slot_v, pks_stream stream) {
+  pks_status st = pks::check_shapes(args);
+  if (st != PKS_OK) return st;
+  if ((st = pks::check_common_ptrs(args)) != PKS_OK) return st;
+  if ((st = pks::check_attn_ptrs(args)) != PKS_OK) return st;
+  if (!state || !slot_k || !slot_v || !residency_sizes_ok(args->num_pages, capacity))
+    return PKS_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(state) & (pks::kAlign - 1)) != 0) return PKS_ERR_INVALID;
+  if (!pks::aligned16(slot_k) || !pks::aligned16(slot_v)) return PKS_ERR_INVALID;
+  const WorkspaceLayout L = pks::workspace_layout(*args);
+  if ((st = pks::check_workspace(args, L)) != PKS_OK) return st;
+  if (args->B == 0) return PKS_OK;
+  const ResidencyLayout R = residency_layout(args->num_pages, capacity);
+  // kv_k / kv_v of the arguments are the host pools; the slots replace them
+  pks_decode_args a = *args;
+  a.kv_k = slot_k;
+  a.kv_v = slot_v;
+  pks::ResidentKv rk;
+  rk.page_slot = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(state) + R.page_slot);
+  rk.capacity = capacity;
+  rk.host_k = static_cast<const __nv_bfloat16*>(args->kv_k);
+  rk.host_v = static_cast<const __nv_bfloat16*>(args->kv_v);
+  return pks::from_cuda(pks::launch_attention(a, L, static_cast<uint8_t*>(args->workspace),
+                                              /*trim=*/false,
+                                              reinterpret_cast<cudaStream_t>(stream), rk));
+}
+
+pks_status pks_residency_fetch(const void* state, int32_t num_pages, int32_t capacity,
+                               const int32_t* miss_list, const int32_t* n_miss,
+                               const void* host_k, const void* host_v, void* slot_k,
+                               void* slot_v, int64_t page_bytes, pks_stream stream) {
+  if (!state || !residency_sizes_ok(num_pages, capacity)) return PKS_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(state) & (pks::kAlign - 1)) != 0) return PKS_ERR_INVALID;
+  if (!miss_list || !n_miss || !host_k || !host_v || !slot_k || !slot_v) return PKS_ERR_INVALID;
+  if (page_bytes < 16 || page_bytes % 16 != 0) return PKS_ERR_INVALID;
+  if (!pks::aligned16(host_k) || !pks::aligned16(host_v) || !pks::aligned16(slot_k) ||
+      !pks::aligned16(slot_v))
+    return PKS_ERR_INVALID;
+  if (capacity == 0) return PKS_OK;
+  const ResidencyLayout R = residency_layout(num_pages, capacity);
+  return pks::from_cuda(pks::launch_residency_fetch(
+      reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(state) + R.page_slot),
+      miss_list, n_miss, static_cast<const uint8_t*>(host_k), static_cast<const uint8_t*>(host_v),
+      static_cast<uint8_t*>(slot_k), static_cast<uint8_t*>(slot_v), page_bytes, num_pages,
+      capacity, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

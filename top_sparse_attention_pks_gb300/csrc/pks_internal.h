@@ -1,6 +1,7 @@
 // Internal declarations shared by the host layer and the kernel files of libpks.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -118,8 +119,24 @@ bool topk_single_launch(const pks_decode_args& a, const WorkspaceLayout& L);
 int topk_kernel_launches(const pks_decode_args& a, const WorkspaceLayout& L);
 // trim: the top-k list holds its selected entries first (the step's own
 // output), so only min(k, len_b) positions per request are visited.
+// K/V through a residency table: kv_k / kv_v of the arguments are then the
+// slot pools [capacity, P, Hkv, D], resident pages are read from their slot,
+// other pages from the host pool (device-accessible host memory).
+struct ResidentKv {
+  const int32_t* page_slot = nullptr;  // nullptr: plain pool
+  int capacity = 0;
+  const __nv_bfloat16* host_k = nullptr;
+  const __nv_bfloat16* host_v = nullptr;
+};
 cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
-                             bool trim, cudaStream_t s);
+                             bool trim, cudaStream_t s, const ResidentKv& rk = ResidentKv{});
+// Copy the admitted misses of the last residency step (miss_list[0..*n_miss)
+// with a slot in page_slot) from the host pools into the slot pools.
+cudaError_t launch_residency_fetch(const int32_t* page_slot, const int32_t* miss_list,
+                                   const int32_t* n_miss, const uint8_t* host_k,
+                                   const uint8_t* host_v, uint8_t* slot_k, uint8_t* slot_v,
+                                   int64_t page_bytes, int num_pages, int capacity,
+                                   cudaStream_t s);
 cudaError_t launch_residency(int32_t* state, int32_t num_pages, int32_t capacity, int32_t B,
                              int32_t k, int32_t page_size, int32_t max_pages,
                              const int32_t* topk_idx, const int32_t* block_table,

@@ -98,6 +98,12 @@ def _declare(L):
     L.pks_decode_step.restype = _ST
     L.pks_sparse_attention_static.argtypes = [_PARGS, _P]
     L.pks_sparse_attention_static.restype = _ST
+    L.pks_decode_select.argtypes = [_PARGS, _P]
+    L.pks_decode_select.restype = _ST
+    L.pks_sparse_attention_resident.argtypes = [_PARGS, _P, _I32, _P, _P, _P]
+    L.pks_sparse_attention_resident.restype = _ST
+    L.pks_residency_fetch.argtypes = [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P]
+    L.pks_residency_fetch.restype = _ST
     L.pks_decode_launches.argtypes = [_PARGS, _P]
     L.pks_decode_launches.restype = _ST
     L.pks_decode_step_timed.argtypes = [_PARGS, _P, _P]
@@ -285,6 +291,34 @@ def pks_decode_launches(args: pks_decode_args) -> int:
     return n.value
 
 
+def pks_decode_select(args: pks_decode_args, stream=None) -> None:
+    """Scan and top-k only (writes args.topk_idx)."""
+    _check(lib().pks_decode_select(ctypes.byref(args), _stream(stream)), "pks_decode_select")
+
+
+def pks_sparse_attention_resident(args: pks_decode_args, state: torch.Tensor, capacity: int,
+                                  slot_k: torch.Tensor, slot_v: torch.Tensor,
+                                  stream=None) -> None:
+    """Attention with K/V through the residency table (args' K/V = host pools)."""
+    _check(lib().pks_sparse_attention_resident(
+        ctypes.byref(args), _dptr(state, torch.uint8, "state"), int(capacity),
+        _dptr(slot_k, torch.bfloat16, "slot_k"), _dptr(slot_v, torch.bfloat16, "slot_v"),
+        _stream(stream)), "pks_sparse_attention_resident")
+
+
+def pks_residency_fetch(state: torch.Tensor, num_pages: int, capacity: int,
+                        miss_list: torch.Tensor, n_miss: torch.Tensor, host_k: torch.Tensor,
+                        host_v: torch.Tensor, slot_k: torch.Tensor, slot_v: torch.Tensor,
+                        page_bytes: int, stream=None) -> None:
+    """Copy the admitted misses of the last residency step into their slots."""
+    _check(lib().pks_residency_fetch(
+        _dptr(state, torch.uint8, "state"), int(num_pages), int(capacity),
+        _dptr(miss_list, torch.int32, "miss_list"), _dptr(n_miss, torch.int32, "n_miss"),
+        _dptr(host_k, torch.bfloat16, "host_k"), _dptr(host_v, torch.bfloat16, "host_v"),
+        _dptr(slot_k, torch.bfloat16, "slot_k"), _dptr(slot_v, torch.bfloat16, "slot_v"),
+        int(page_bytes), _stream(stream)), "pks_residency_fetch")
+
+
 def pks_decode_step(args: pks_decode_args, stream=None) -> None:
     _check(lib().pks_decode_step(ctypes.byref(args), _stream(stream)), "pks_decode_step")
 
@@ -372,6 +406,12 @@ class ResidencyTable:
     def update(self, topk_idx, block_table, page_size, miss_list, n_miss, stream=None):
         pks_residency_update(self.state, self.num_pages, self.capacity, page_size, topk_idx,
                              block_table, miss_list, n_miss, stream)
+
+    def fetch(self, miss_list, n_miss, host_k, host_v, slot_k, slot_v, stream=None):
+        """Copy the admitted misses of the last update from the host pools into their slots."""
+        page_bytes = host_k[0].numel() * host_k.element_size()
+        pks_residency_fetch(self.state, self.num_pages, self.capacity, miss_list, n_miss, host_k,
+                            host_v, slot_k, slot_v, page_bytes, stream)
 
     def _i32(self, name, n):
         off = self.offsets[name]
