@@ -222,6 +222,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests (smaller profiling case)")
+    ap.add_argument("--topk", type=int, default=0, help="override the workload's k")
+    ap.add_argument("--hisparse", action="store_true",
+                    help="workloads with a slot table: K/V in pinned host memory, HBM slots, "
+                         "misses fetched every step (select, update, fetch, attention)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -247,6 +251,8 @@ def main():
     wl = WORKLOADS[args.workload]
     if args.requests:
         wl = shrink(wl, args.requests)
+    if args.topk:
+        wl = wl.replace(k=args.topk)
     t, h, bt = setup(wl, dev, seed_offset=rank)
 
     if args.impl == "reference":
@@ -261,6 +267,14 @@ def main():
                 "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    if args.hisparse:
+        if wl.capacity <= 0:
+            ap.error("--hisparse needs a workload with a slot table")
+        hisparse_bench(wl, t, h, args, dev, rank)
         if dist:
             dist.destroy_process_group()
         return
@@ -411,6 +425,79 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def hisparse_bench(wl, t, h, args, dev, rank):
+    """The decode step with the KV cache in pinned host memory and an LRU cache
+    of its pages in HBM: select, residency update, miss fetch, attention
+    through the table.  Prints one JSON line (rank 0)."""
+    from top_sparse_attention_pks_gb300.decoder import ResidentDecodeStep
+    host_k = t["kv_k"].cpu().pin_memory()
+    host_v = t["kv_v"].cpu().pin_memory()
+    t = dict(t)
+    del t["kv_k"], t["kv_v"]  # the pools now live in host memory only
+    torch.cuda.empty_cache()
+    rs = ResidentDecodeStep(t, host_k, host_v, wl.k, wl.capacity,
+                            h["initial_resident"].numpy())
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    page_bytes = host_k[0].numel() * host_k.element_size()
+    # a decode step brings a new indexer query: cycle through 8 seeded ones
+    # (copied into place before each step, outside the timed interval)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    q_var = [torch.randint(-127, 128, t["q_idx"].shape, dtype=torch.int8, device=dev,
+                           generator=gen) for _ in range(8)]
+    with torch.cuda.stream(s):
+        for i in range(args.warmup):
+            t["q_idx"].copy_(q_var[i % 8])
+            rs(s)
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    fetched = []
+    for i in range(n):
+        with torch.cuda.stream(s):
+            t["q_idx"].copy_(q_var[(args.warmup + i) % 8])
+            flush.zero_()
+            e = ev[i]
+            e[0].record(s)
+            pks.pks_decode_select(rs.args, s)
+            e[1].record(s)
+            rs.table.update(rs.step.topk_idx, rs.block_table, rs.page_size, rs.miss, rs.n_miss, s)
+            e[2].record(s)
+            rs.table.fetch(rs.miss, rs.n_miss, rs.host_k, rs.host_v, rs.slot_k, rs.slot_v, s)
+            e[3].record(s)
+            pks.pks_sparse_attention_resident(rs.args, rs.table.state, rs.capacity, rs.slot_k,
+                                              rs.slot_v, s)
+            e[4].record(s)
+        if i < 20:  # admitted misses of this step (slots that now hold a missed page)
+            torch.cuda.synchronize()
+            nm = int(rs.n_miss.item())
+            ps = rs.table.page_slot()[rs.miss[:nm].long()]
+            fetched.append(int((ps >= 0).sum().item()))
+    torch.cuda.synchronize()
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])
+    med = np.median(stage, axis=0)
+    step_ms = float(np.median(stage.sum(axis=1)))
+    fetch_pages = float(np.mean(fetched))
+    fetch_bytes = 2 * fetch_pages * page_bytes
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": 1e3 / step_ms, "unit": UNIT, "n_gpus": 1,
+            "steps": n, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": dict(config_dict(wl, args), kv_pools="pinned host memory",
+                           hbm_slots=wl.capacity),
+            "stages_ms": {"select": med[0], "residency_update": med[1], "fetch": med[2],
+                          "attention": med[3]},
+            "fetch": {"pages_per_step": fetch_pages, "bytes_per_step": fetch_bytes,
+                      "gbs": fetch_bytes / (med[2] * 1e-3) / 1e9},
+            "timing": "CUDA events between the four calls, L2 write-flushed before each step",
+            "queries": "a new seeded indexer query each step (8 in rotation)",
+        }), flush=True)
 
 
 def job_throughput(local_s, steps, world, dist=None, device="cpu"):
