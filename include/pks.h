@@ -111,6 +111,19 @@ pks_status pks_build_block_table(pks_pool* pool, int32_t batch, const int32_t* s
                                  const int32_t* prefix_group, int32_t prefix_len,
                                  int32_t max_pages, int32_t* block_table, int32_t* pages_used);
 
+/* Admission on the pool's free pages ([PKV] "How many users" and "Internal
+ * fragmentation").  Requests of lengths lens[i % n] (i = 0, 1, ...) arrive
+ * and never finish; each takes ceil(len / page_size) pages (reserve == 0:
+ * paging) or ceil(reserve / page_size) pages (reserve > 0: every request
+ * reserves `reserve` tokens, and one longer than that stops admission).
+ * Admission stops at the first request that does not fit.  Writes *admitted,
+ * *tokens (the admitted lengths' sum) and *slots (pages taken x page_size);
+ * waste = slots - tokens.  Counts only: the pool is not modified.  INVALID on
+ * a negative length or when the requests take no pages (unbounded). */
+pks_status pks_admission_simulate(const pks_pool* pool, int32_t n, const int32_t* lens,
+                                  int32_t reserve, int64_t* admitted, int64_t* tokens,
+                                  int64_t* slots);
+
 /* ------------------------------------------------------------------------
  * Decode step ([SA] introduction and DeepSeek Sparse Attention paragraph).
  *

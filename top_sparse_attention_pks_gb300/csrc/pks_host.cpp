@@ -205,6 +205,35 @@ pks_status pks_pool_free_count(const pks_pool* pool, int32_t* out) {
   return PKS_OK;
 }
 
+pks_status pks_admission_simulate(const pks_pool* pool, int32_t n, const int32_t* lens,
+                                  int32_t reserve, int64_t* admitted, int64_t* tokens,
+                                  int64_t* slots) {
+  if (!pool || n < 1 || !lens || reserve < 0 || !admitted || !tokens || !slots)
+    return PKS_ERR_INVALID;
+  const int64_t P = pool->page_size;
+  int64_t cycle_pages = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (lens[i] < 0) return PKS_ERR_INVALID;
+    cycle_pages += reserve > 0 ? (reserve + P - 1) / P : (lens[i] + P - 1) / P;
+  }
+  if (cycle_pages == 0) return PKS_ERR_INVALID;  // requests that take no pages: unbounded
+  const int64_t free_pages = (int64_t)pool->free_list.size();
+  int64_t used = 0, adm = 0, tok = 0;
+  for (int64_t i = 0;; ++i) {
+    const int32_t len = lens[i % n];
+    if (reserve > 0 && len > reserve) break;  // does not fit its reservation
+    const int64_t need = reserve > 0 ? (reserve + P - 1) / P : (len + P - 1) / P;
+    if (used + need > free_pages) break;
+    used += need;
+    tok += len;
+    ++adm;
+  }
+  *admitted = adm;
+  *tokens = tok;
+  *slots = used * P;
+  return PKS_OK;
+}
+
 pks_status pks_alloc_pages(pks_pool* pool, int32_t n, int32_t* out_ids) {
   if (!pool || n < 0 || (n > 0 && !out_ids)) return PKS_ERR_INVALID;
   if ((size_t)n > pool->free_list.size()) return PKS_ERR_OOM;

@@ -88,6 +88,8 @@ def _declare(L):
     L.pks_alloc_pages.restype = _ST
     L.pks_free_pages.argtypes = [_P, _I32, _P]
     L.pks_free_pages.restype = _ST
+    L.pks_admission_simulate.argtypes = [_P, _I32, _P, _I32, _P, _P, _P]
+    L.pks_admission_simulate.restype = _ST
     L.pks_build_block_table.argtypes = [_P, _I32, _P, _P, _I32, _I32, _P, _P]
     L.pks_build_block_table.restype = _ST
     L.pks_decode_workspace_size.argtypes = [_PARGS, ctypes.POINTER(ctypes.c_size_t)]
@@ -205,6 +207,17 @@ def pks_build_block_table(pool: int, seq_lens, max_pages: int, prefix_group=None
     return bt, used.value
 
 
+def pks_admission_simulate(pool: int, lens, reserve: int = 0):
+    """``(admitted, tokens, slots)`` of cyclic admission on the pool's free pages
+    (reserve 0: paging; reserve > 0: every request reserves that many tokens)."""
+    a = _host_i32(lens)
+    adm, tok, slots = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().pks_admission_simulate(pool, a.shape[0], a.ctypes.data, int(reserve),
+                                        ctypes.addressof(adm), ctypes.addressof(tok),
+                                        ctypes.addressof(slots)), "pks_admission_simulate")
+    return adm.value, tok.value, slots.value
+
+
 class Pool:
     """Owning wrapper of a host page pool handle."""
 
@@ -222,6 +235,9 @@ class Pool:
 
     def build_block_table(self, seq_lens, max_pages, prefix_group=None, prefix_len=0):
         return pks_build_block_table(self.handle, seq_lens, max_pages, prefix_group, prefix_len)
+
+    def admission(self, lens, reserve: int = 0):
+        return pks_admission_simulate(self.handle, lens, reserve)
 
     def close(self):
         if self.handle:
