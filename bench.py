@@ -66,23 +66,30 @@ def setup(wl, device, seed_offset=0):
 
 def algorithmic_bytes(wl, lens, bt, topk):
     """Unique physical bytes of one step: indexer keys scanned, K/V rows
-    gathered, outputs written (aliased prefix pages counted once)."""
+    gathered, outputs written (aliased prefix pages counted once).  With
+    several query tokens per request (topk [B, Nq, k]) every query's gather
+    counts: rows are unique within a query's selections, summed over queries."""
     P = wl.page_size
-    scan_rows, kv_rows = [], []
+    topk = np.asarray(topk)
+    if topk.ndim == 2:
+        topk = topk[:, None, :]
+    nq = topk.shape[1]
+    scan_rows, kv_rows = [], [[] for _ in range(nq)]
     for b, n in enumerate(lens):
         n = int(n)
         if n == 0:
             continue
         t = np.arange(n, dtype=np.int64)
         scan_rows.append(bt[b, t // P].astype(np.int64) * P + t % P)
-        sel = topk[b][topk[b] >= 0].astype(np.int64)
-        kv_rows.append(bt[b, sel // P].astype(np.int64) * P + sel % P)
+        for q in range(nq):
+            sel = topk[b, q][topk[b, q] >= 0].astype(np.int64)
+            kv_rows[q].append(bt[b, sel // P].astype(np.int64) * P + sel % P)
     n_scan = np.unique(np.concatenate(scan_rows)).size if scan_rows else 0
-    n_kv = np.unique(np.concatenate(kv_rows)).size if kv_rows else 0
+    n_kv = sum(np.unique(np.concatenate(r)).size for r in kv_rows if r)
     scan = n_scan * wl.Di
     kv = n_kv * wl.Hkv * wl.D * 2 * 2
-    out = wl.B * wl.Hq * wl.D * 2
-    attended = int(sum(min(int(n), wl.k) for n in lens))
+    out = wl.B * nq * wl.Hq * wl.D * 2
+    attended = nq * int(sum(min(int(n), wl.k) for n in lens))
     return dict(scan=scan, kv=kv, out=out, total=scan + kv + out, attended=attended)
 
 
@@ -223,6 +230,8 @@ def main():
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests (smaller profiling case)")
     ap.add_argument("--topk", type=int, default=0, help="override the workload's k")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="query tokens per request (each scores, selects and attends alone)")
     ap.add_argument("--hisparse", action="store_true",
                     help="workloads with a slot table: K/V in pinned host memory, HBM slots, "
                          "misses fetched every step (select, update, fetch, attention)")
@@ -254,6 +263,15 @@ def main():
     if args.topk:
         wl = wl.replace(k=args.topk)
     t, h, bt = setup(wl, dev, seed_offset=rank)
+    if args.queries > 1:
+        # Nq query tokens per request: seeded queries of shape [B, Nq, ...]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(2000 + rank)
+        t["q"] = torch.randn((wl.B, args.queries, wl.Hq, wl.D), device=dev,
+                             generator=gen).to(torch.bfloat16)
+        t["q_idx"] = torch.randint(-127, 128, (wl.B, args.queries, wl.Hi, wl.Di),
+                                   dtype=torch.int8, device=dev, generator=gen)
+        args.no_cpu_baseline = True
 
     if args.impl == "reference":
         ref = time_oracle(wl, t, budget_s=120.0, steps=args.steps, warmup=args.warmup)
@@ -531,6 +549,7 @@ def config_dict(wl, args):
             "page_size": wl.page_size, "heads_q_kv": [wl.Hq, wl.Hkv], "head_dim": wl.D,
             "indexer_heads_dim": [wl.Hi, wl.Di], "indexer_dtype": "int8", "top_k": wl.k,
             "kv_dtype": "bf16", "prefix": [wl.prefix_len, wl.group_size],
+            "query_tokens": getattr(args, "queries", 1),
             "residency_slots": wl.capacity, "parallelism": f"replicas x{args.gpus}",
             "l2": "flushed between timed steps (256 MB write, outside the timed intervals)",
             "timing": "CUDA events around each CUDA-graph replay of the step"}

@@ -164,7 +164,14 @@ typedef struct pks_decode_args {
                              of all selected (KV head group, request, position) work */
   int32_t topk_mode;      /* 0 = one cooperative top-k launch when its grid fits on the GPU
                              at once, else two; 1 = always the two-kernel path */
-  int32_t reserved[2];    /* must be 0 */
+  int32_t n_queries;      /* query tokens per request, Nq (0 or 1: one).  With Nq > 1, q is
+                             [B, Nq, Hq, D], q_idx [B, Nq, Hi, Di], topk_idx [B, Nq, k] and
+                             out [B, Nq, Hq, D]: every query token of request b scores the
+                             request's len_b cached tokens, selects its own top-k and attends
+                             over it; the indexer keys are read once for all Nq queries.
+                             Nq in {1, 2, 4, 8} and Hi * Nq <= 8 (UNSUPPORTED otherwise);
+                             pks_indexer_scores then writes B * Nq score rows */
+  int32_t reserved[1];    /* must be 0 */
 } pks_decode_args;
 
 /* Workspace bytes a step with these shapes needs (pointers may be NULL). */

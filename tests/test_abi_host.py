@@ -166,13 +166,14 @@ def test_workspace_size_and_validation_without_gpu():
     # no workspace -> PKS_ERR_WORKSPACE, before any device work
     assert L.pks_decode_step(ctypes.byref(a), None) == -7
     cases = [dict(Hq=6, Hkv=4), dict(k=0), dict(page_size=0), dict(B=-1),
-             dict(reserved=(ctypes.c_int32 * 2)(1, 0)), dict(topk_mode=2), dict(topk_mode=-1), dict(attn_splits=-2),
+             dict(reserved=(ctypes.c_int32 * 1)(1)), dict(topk_mode=2), dict(topk_mode=-1), dict(n_queries=-1), dict(attn_splits=-2),
              dict(attn_splits=1025)]
     for c in cases:
         assert L.pks_decode_workspace_size(ctypes.byref(_cpu_args(**c)),
                                            ctypes.byref(ctypes.c_size_t())) == -1, c
     unsupported = [dict(D=96), dict(Di=32), dict(Hi=3), dict(Hq=64, Hkv=2), dict(B=5000),
-                   dict(k=70000)]
+                   dict(k=70000), dict(n_queries=3), dict(Hi=4, n_queries=4),
+                   dict(B=1025, n_queries=4)]
     for c in unsupported:
         assert L.pks_decode_workspace_size(ctypes.byref(_cpu_args(**c)),
                                            ctypes.byref(ctypes.c_size_t())) == -6, c

@@ -116,7 +116,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
                    float* __restrict__ part_o, __nv_bfloat16* __restrict__ out,
                    int32_t* __restrict__ err, int B, int Hq, int Hkv, int G, int page_size,
                    int max_pages, int num_pages, int k, int trim, int min_per_cta,
-                   float scale_log2, ResidentKv rk) {
+                   float scale_log2, ResidentKv rk, int nq) {
   constexpr int NT = HG * 32;
   constexpr int CH = D / 8;   // 16-byte chunks per head row
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
@@ -144,7 +144,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     for (int i = 0; i < per; ++i) {
       const int b = tid * per + i;
       if (b < B) {
-        const int len = seq_lens[b];
+        const int len = seq_lens[b / nq];  // b: virtual request
         local += (len < 0 || len > max_len) ? 0 : (trim ? min(len, k) : k);
       }
     }
@@ -162,7 +162,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
       const int b = tid * per + i;
       if (b < B) {
         s_prefix[b] = before;
-        const int len = seq_lens[b];
+        const int len = seq_lens[b / nq];  // b: virtual request
         before += (len < 0 || len > max_len) ? 0 : (trim ? min(len, k) : k);
       }
     }
@@ -281,7 +281,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     auto resolve_rows = [&](int64_t f0, int64_t f1) {
       for (int64_t f = f0 + tid; f < f1; f += NT) {
         const SegCursor c = locate(f);
-        int len = seq_lens[c.b];
+        int len = seq_lens[c.b / nq];
         if (len < 0 || len > max_len) len = 0;
         const int t = topk[(int64_t)c.b * k + c.p];
         int row = -1;
@@ -289,7 +289,7 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
           if (t >= len) {
             flag_error(err, kErrToken);
           } else {
-            const int page = block_table[(int64_t)c.b * max_pages + t / page_size];
+            const int page = block_table[(int64_t)(c.b / nq) * max_pages + t / page_size];
             if ((unsigned)page < (unsigned)num_pages) {
               row = page * page_size + t % page_size;
               if (rk.page_slot != nullptr) {
@@ -548,7 +548,9 @@ template <int D, int HG>
 cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
                           bool trim, const ResidentKv& rk, cudaStream_t s) {
   auto kern = k_sparse_attention<D, HG>;
-  const size_t smem = attn_smem_bytes<D, HG>(a.B);
+  const int nq = query_count(a);
+  const int Bv = a.B * nq;  // virtual requests
+  const size_t smem = attn_smem_bytes<D, HG>(Bv);
   // raise the dynamic shared-memory limit once per device and size (not a
   // stream operation, so it stays out of any graph capture after the first call)
   static size_t configured[64] = {0};
@@ -576,15 +578,15 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
       reinterpret_cast<const __nv_bfloat16*>(a.kv_k), reinterpret_cast<const __nv_bfloat16*>(a.kv_v),
       (const int32_t*)a.topk_idx, reinterpret_cast<int32_t*>(ws + L.attn_prefix),
       reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
-      reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.B, a.Hq,
+      reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), Bv, a.Hq,
       a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, trim ? 1 : 0, min_per_cta,
-      scale_log2, rk);
+      scale_log2, rk, nq);
   if (e != cudaSuccess) return e;
-  return launch_ex(k_attention_merge<D>, dim3((a.Hq + 3) / 4, a.B), dim3(128), 0, s, true, false,
+  return launch_ex(k_attention_merge<D>, dim3((a.Hq + 3) / 4, Bv), dim3(128), 0, s, true, false,
                    reinterpret_cast<const int32_t*>(ws + L.attn_prefix),
                    reinterpret_cast<const float2*>(ws + L.part_ml),
                    reinterpret_cast<const float*>(ws + L.part_o),
-                   reinterpret_cast<__nv_bfloat16*>(a.out), a.B, a.Hq, a.Hkv, (int)HG, G, grid,
+                   reinterpret_cast<__nv_bfloat16*>(a.out), Bv, a.Hq, a.Hkv, (int)HG, G, grid,
                    min_per_cta);
 }
 
@@ -603,14 +605,15 @@ StaticAttnLayout static_attn_layout(const pks_decode_args& a, int64_t grid) {
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const int hg = attn_heads_per_cta(a.Hkv);
   const int G = a.Hq / a.Hkv;
-  const int64_t nseg = (int64_t)(a.Hkv / hg) * a.B;
+  const int64_t Bv = (int64_t)a.B * query_count(a);
+  const int64_t nseg = (int64_t)(a.Hkv / hg) * Bv;
   const size_t nslots = (size_t)(grid + nseg) * hg * G;
   StaticAttnLayout L{};
   size_t off = 0;
   L.err = off;
   off = up(off + sizeof(int32_t) * 4);
   L.attn_prefix = off;
-  off = up(off + sizeof(int32_t) * (size_t)(a.B + 1));
+  off = up(off + sizeof(int32_t) * (size_t)(Bv + 1));
   L.part_ml = off;
   off = up(off + sizeof(float) * 2 * nslots);
   L.part_o = off;
@@ -623,7 +626,9 @@ template <int D, int HG>
 cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cudaStream_t s,
                                  bool* too_large) {
   auto kern = k_sparse_attention<D, HG>;
-  const size_t smem = attn_smem_bytes<D, HG>(a.B);
+  const int nq = query_count(a);
+  const int Bv = a.B * nq;
+  const size_t smem = attn_smem_bytes<D, HG>(Bv);
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -646,16 +651,16 @@ cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cud
       reinterpret_cast<const __nv_bfloat16*>(a.kv_k), reinterpret_cast<const __nv_bfloat16*>(a.kv_v),
       a.topk_idx, reinterpret_cast<int32_t*>(scratch + L.attn_prefix),
       reinterpret_cast<float2*>(scratch + L.part_ml), reinterpret_cast<float*>(scratch + L.part_o),
-      reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(scratch + L.err), a.B,
+      reinterpret_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(scratch + L.err), Bv,
       a.Hq, a.Hkv, G, a.page_size, a.max_pages, a.num_pages, a.k, /*trim=*/0, min_per_cta,
-      scale_log2, ResidentKv{});
+      scale_log2, ResidentKv{}, nq);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_attention_merge<D><<<dim3((a.Hq + 3) / 4, a.B), 128, 0, s>>>(
+  k_attention_merge<D><<<dim3((a.Hq + 3) / 4, Bv), 128, 0, s>>>(
       reinterpret_cast<const int32_t*>(scratch + L.attn_prefix),
       reinterpret_cast<const float2*>(scratch + L.part_ml),
       reinterpret_cast<const float*>(scratch + L.part_o), reinterpret_cast<__nv_bfloat16*>(a.out),
-      a.B, a.Hq, a.Hkv, HG, G, grid, min_per_cta);
+      Bv, a.Hq, a.Hkv, HG, G, grid, min_per_cta);
   return cudaGetLastError();
 }
 

@@ -94,22 +94,24 @@ __device__ __forceinline__ void imma_16832(int (&c)[4], int a0, int a1, int a2, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int HI, int DI, int NT>
+template <int HI, int DI, int NT, int NQ>
 __global__ void __launch_bounds__(NT, 1)
 k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                    const int8_t* __restrict__ q_idx, const int32_t* __restrict__ w_idx,
                    const int8_t* __restrict__ idx_k, int32_t* __restrict__ scores, int64_t ld,
                    int32_t* __restrict__ hist, int32_t* __restrict__ err, int B, int max_pages,
                    int page_size, int page_shift, int num_pages, int k) {
-  static_assert(HI <= 8, "N = 8 heads per MMA");
+  static_assert(HI * NQ <= 8, "N = 8 query heads per MMA");
   constexpr int HALVES = DI / 64;      // 64-byte halves of a key (2 or 1)
   constexpr int NLD = 2 * 2 * HALVES;  // loads per lane per 32-token round
 
   extern __shared__ int smem_i[];
   // the top-k grid may take SM slots as soon as this grid's CTAs retire
   pdl_launch_dependents();
-  int* s_hist = smem_i;                 // [kScoreBins]
-  int* s_prefix = smem_i + kScoreBins;  // [B + 1]
+  int* s_hist = smem_i;                      // [NQ][kScoreBins]
+  int* s_prefix = smem_i + NQ * kScoreBins;  // [B + 1]
+  // NQ > 1: weighted ReLU of each (token, query head) of a warp's round
+  __shared__ int s_ep[NQ > 1 ? NT / 32 : 1][32][8];
   __shared__ int s_warp[NT / 32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -141,7 +143,7 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     }
   }
   if (tid == 0) s_prefix[B] = total_rounds;
-  for (int i = tid; i < kScoreBins; i += NT) s_hist[i] = 0;
+  for (int i = tid; i < NQ * kScoreBins; i += NT) s_hist[i] = 0;
   __syncthreads();
 
   const int64_t G = gridDim.x;
@@ -215,8 +217,9 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     return row;
   };
 
-  int4 qf[HALVES];  // chunks 4*hv + tq of head gq (zero for padded heads)
-  int w0 = 0, w1 = 0;  // weights of heads 2tq and 2tq+1
+  // query head n of the MMA's N = 8 columns: query n / HI, indexer head n % HI
+  int4 qf[HALVES];  // chunks 4*hv + tq of query head gq (zero for padding)
+  int w0 = 0, w1 = 0;  // weights of query heads 2tq and 2tq+1
   int cb = -1, cb_len = 0, cb_first = 0, cb_next = 0;
   bool do_hist = false;
   // output token of this lane: tile (tq >> 1), row gq + 8 * (tq & 1)
@@ -228,8 +231,9 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
       while (s_prefix[b + 1] <= item) ++b;
       if (do_hist) {
         __syncthreads();
-        int32_t* gh = hist + (int64_t)cb * kScoreBins;
-        for (int i = tid; i < kScoreBins; i += NT) {
+        // request cb's queries are virtual requests cb * NQ .. cb * NQ + NQ - 1
+        int32_t* gh = hist + (int64_t)cb * NQ * kScoreBins;
+        for (int i = tid; i < NQ * kScoreBins; i += NT) {
           const int cnt = s_hist[i];
           if (cnt) {
             atomicAdd(gh + i, cnt);
@@ -244,15 +248,49 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
       const int len = seq_lens[b];
       cb_len = (len < 0 || len > max_len) ? 0 : len;
       do_hist = hist != nullptr && cb_len > k;
+      // q_idx is [B, NQ, HI, DI]: query head n of request b is row b * NQ * HI + n
 #pragma unroll
       for (int hv = 0; hv < HALVES; ++hv)
-        qf[hv] = gq < HI ? __ldg(reinterpret_cast<const int4*>(q_idx + ((int64_t)b * HI + gq) * DI) +
-                                 4 * hv + tq)
-                         : make_int4(0, 0, 0, 0);
-      w0 = 2 * tq < HI ? __ldg(w_idx + 2 * tq) : 0;
-      w1 = 2 * tq + 1 < HI ? __ldg(w_idx + 2 * tq + 1) : 0;
+        qf[hv] = gq < HI * NQ
+                     ? __ldg(reinterpret_cast<const int4*>(q_idx + ((int64_t)b * NQ * HI + gq) * DI) +
+                             4 * hv + tq)
+                     : make_int4(0, 0, 0, 0);
+      w0 = 2 * tq < HI * NQ ? __ldg(w_idx + (2 * tq) % HI) : 0;
+      w1 = 2 * tq + 1 < HI * NQ ? __ldg(w_idx + (2 * tq + 1) % HI) : 0;
     }
 
+    if constexpr (NQ > 1) {
+      // weighted ReLU of every (token, query head) into the warp's tile; then
+      // lane L sums the HI heads of each query for token L of the round
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        int c[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int hv = 0; hv < HALVES; ++hv) {
+          const int4 r0 = buf[(u * HALVES + hv) * 2 + 0];
+          const int4 r1 = buf[(u * HALVES + hv) * 2 + 1];
+          imma_16832<DI>(c, r0.x, r1.x, r0.y, r1.y, qf[hv].x, qf[hv].y);
+          imma_16832<DI>(c, r0.z, r1.z, r0.w, r1.w, qf[hv].z, qf[hv].w);
+        }
+        s_ep[warp][u * 16 + gq][2 * tq] = w0 * max(c[0], 0);
+        s_ep[warp][u * 16 + gq][2 * tq + 1] = w1 * max(c[1], 0);
+        s_ep[warp][u * 16 + gq + 8][2 * tq] = w0 * max(c[2], 0);
+        s_ep[warp][u * 16 + gq + 8][2 * tq + 1] = w1 * max(c[3], 0);
+      }
+      __syncwarp();
+      const int t = (item - cb_first) * NT + warp * 32 + lane;
+      const bool valid = t < cb_len;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        int score = 0;
+#pragma unroll
+        for (int h = 0; h < HI; ++h) score += s_ep[warp][lane][q * HI + h];
+        if (valid) store_score_keep(scores + ((int64_t)cb * NQ + q) * ld + t, score);
+        if (do_hist && valid) atomicAdd(&s_hist[q * kScoreBins + score_bin(score)], 1);
+      }
+      __syncwarp();  // the tile is rewritten next round
+      return;
+    }
     int sc[2][2];  // [tile][row g / g+8]
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -293,8 +331,8 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   }
   if (do_hist) {
     __syncthreads();
-    int32_t* gh = hist + (int64_t)cb * kScoreBins;
-    for (int i = tid; i < kScoreBins; i += NT) {
+    int32_t* gh = hist + (int64_t)cb * NQ * kScoreBins;
+    for (int i = tid; i < NQ * kScoreBins; i += NT) {
       const int cnt = s_hist[i];
       if (cnt) atomicAdd(gh + i, cnt);
     }
@@ -318,7 +356,7 @@ cudaError_t raise_smem(K kern, size_t smem, size_t (&configured)[64]) {
 // threads a CTA (one CTA an SM)
 constexpr int kMmaThreads = 1024;
 
-template <int HI, int DI>
+template <int HI, int DI, int NQ>
 cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld, int32_t* hist,
                           int32_t* err, cudaStream_t s) {
   int shift = -1;
@@ -327,33 +365,46 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
     while ((1 << shift) < a.page_size) ++shift;
   }
   static size_t configured[64] = {0};  // per instantiation
-  const size_t smem = sizeof(int) * ((size_t)kScoreBins + a.B + 1);
-  auto go = [&](auto kern, int threads) {
-    cudaError_t e = raise_smem(kern, smem, configured);
-    if (e != cudaSuccess) return e;
-    kern<<<device_sm_count(), threads, smem, s>>>(a.seq_lens, a.block_table, a.q_idx, a.w_idx,
-                                                  a.idx_k, scores, ld, hist, err, a.B,
-                                                  a.max_pages, a.page_size, shift, a.num_pages,
-                                                  a.k);
-    return cudaGetLastError();
-  };
-  return go(k_indexer_scan_mma<HI, DI, kMmaThreads>, kMmaThreads);
+  const size_t smem = sizeof(int) * ((size_t)NQ * kScoreBins + a.B + 1);
+  auto kern = k_indexer_scan_mma<HI, DI, kMmaThreads, NQ>;
+  cudaError_t e = raise_smem(kern, smem, configured);
+  if (e != cudaSuccess) return e;
+  kern<<<device_sm_count(), kMmaThreads, smem, s>>>(a.seq_lens, a.block_table, a.q_idx, a.w_idx,
+                                                    a.idx_k, scores, ld, hist, err, a.B,
+                                                    a.max_pages, a.page_size, shift, a.num_pages,
+                                                    a.k);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_indexer_scan(const pks_decode_args& a, int32_t* scores, int64_t ld,
                                 int32_t* hist, int32_t* err, cudaStream_t s) {
-#define PKS_SCAN_CASE(HI_, DI_) \
-  if (a.Hi == HI_ && a.Di == DI_) return launch_scan_t<HI_, DI_>(a, scores, ld, hist, err, s);
-  PKS_SCAN_CASE(1, 64)
-  PKS_SCAN_CASE(2, 64)
-  PKS_SCAN_CASE(4, 64)
-  PKS_SCAN_CASE(8, 64)
-  PKS_SCAN_CASE(1, 128)
-  PKS_SCAN_CASE(2, 128)
-  PKS_SCAN_CASE(4, 128)
-  PKS_SCAN_CASE(8, 128)
+  const int nq = query_count(a);
+#define PKS_SCAN_CASE(HI_, DI_, NQ_)                       \
+  if (a.Hi == HI_ && a.Di == DI_ && nq == NQ_)             \
+    return launch_scan_t<HI_, DI_, NQ_>(a, scores, ld, hist, err, s);
+  PKS_SCAN_CASE(1, 64, 1)
+  PKS_SCAN_CASE(2, 64, 1)
+  PKS_SCAN_CASE(4, 64, 1)
+  PKS_SCAN_CASE(8, 64, 1)
+  PKS_SCAN_CASE(1, 128, 1)
+  PKS_SCAN_CASE(2, 128, 1)
+  PKS_SCAN_CASE(4, 128, 1)
+  PKS_SCAN_CASE(8, 128, 1)
+  // several query tokens per request (Hi * Nq <= 8)
+  PKS_SCAN_CASE(1, 64, 2)
+  PKS_SCAN_CASE(1, 64, 4)
+  PKS_SCAN_CASE(1, 64, 8)
+  PKS_SCAN_CASE(2, 64, 2)
+  PKS_SCAN_CASE(2, 64, 4)
+  PKS_SCAN_CASE(4, 64, 2)
+  PKS_SCAN_CASE(1, 128, 2)
+  PKS_SCAN_CASE(1, 128, 4)
+  PKS_SCAN_CASE(1, 128, 8)
+  PKS_SCAN_CASE(2, 128, 2)
+  PKS_SCAN_CASE(2, 128, 4)
+  PKS_SCAN_CASE(4, 128, 2)
 #undef PKS_SCAN_CASE
   return cudaErrorInvalidValue;
 }

@@ -394,14 +394,14 @@ __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_
 __global__ void __launch_bounds__(kTopkThreads, 4)
 k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ scores,
               int64_t ld, TopkWs w, int2* __restrict__ chunk_cnt, int32_t* __restrict__ topk,
-              int k, int max_len, int nchunks_max) {
+              int k, int max_len, int nchunks_max, int nq) {
   __shared__ uint64_t s_key[kCandCap];
   __shared__ int s_eqoff[kTopkCoopMaxChunks + 1];  // candidates before each chunk
   __shared__ int s_before, s_lo, s_hi;
   __shared__ TopkSmem sm;
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   const int start = c * kTopkChunk;
-  const int len = clamp_len(seq_lens[b], max_len);
+  const int len = clamp_len(seq_lens[b / nq], max_len);  // b: virtual request
   pdl_wait();  // scores and histogram come from the scan
 
   // all loads of the chunk phase at once: this thread's 16 scores (rows
@@ -656,7 +656,7 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
 __global__ void __launch_bounds__(kTopkThreads)
 k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ scores,
                  int64_t ld, TopkWs w, int32_t* __restrict__ topk, int k, int max_len,
-                 int nchunks_max) {
+                 int nchunks_max, int nq) {
   extern __shared__ __align__(16) uint8_t dsm[];
   // [kCandCap] staged candidate keys | [kBitmapTokens/32] bitmap | [nchunks] counts
   uint64_t* s_key = reinterpret_cast<uint64_t*>(dsm);
@@ -666,7 +666,7 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
   __shared__ int s_last;
 
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  const int len = clamp_len(seq_lens[b], max_len);
+  const int len = clamp_len(seq_lens[b / nq], max_len);  // b: virtual request
   pdl_wait();  // scores and histogram come from the scan
   pdl_launch_dependents();
   int32_t* row = topk + (int64_t)b * k;
@@ -796,11 +796,11 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
 __global__ void __launch_bounds__(kTopkThreads)
 k_topk_emit(const int32_t* __restrict__ seq_lens, const uint32_t* __restrict__ bits,
             const int32_t* __restrict__ chunk_off, int32_t* __restrict__ topk, int k,
-            int max_len, int nchunks_max) {
+            int max_len, int nchunks_max, int nq) {
   __shared__ int s_warp[kTopkThreads / 32];
   constexpr int kWords = kTopkChunk / 32;  // 128 words per chunk
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  const int len = clamp_len(seq_lens[b], max_len);
+  const int len = clamp_len(seq_lens[b / nq], max_len);  // b: virtual request
   pdl_wait();  // bitmap and offsets come from k_topk_threshold
   pdl_launch_dependents();
   if (len <= k || len <= kBitmapTokens) return;  // written by the threshold kernel
@@ -862,13 +862,14 @@ int64_t select_capacity() {
 
 bool topk_single_launch(const pks_decode_args& a, const WorkspaceLayout& L) {
   return a.topk_mode == 0 && L.nchunks <= kTopkCoopMaxChunks &&
-         (int64_t)L.nchunks * a.B <= select_capacity();
+         (int64_t)L.nchunks * a.B * query_count(a) <= select_capacity();
 }
 
 cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
                         cudaStream_t s) {
   const int max_len = a.max_pages * a.page_size;
-  const dim3 grid(L.nchunks, a.B);
+  const int nq = query_count(a);
+  const dim3 grid(L.nchunks, a.B * nq);  // virtual requests
   const TopkWs w = topk_ws(L, ws);
   const int32_t* scores = reinterpret_cast<const int32_t*>(ws + L.scores);
   if (topk_single_launch(a, L)) {
@@ -876,7 +877,7 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
     // that cannot all be resident
     return launch_ex(k_topk_select, grid, dim3(kTopkThreads), 0, s, /*pdl=*/true, /*coop=*/true,
                      a.seq_lens, scores, L.ld, w, reinterpret_cast<int2*>(ws + L.chunk_cnt),
-                     a.topk_idx, a.k, max_len, (int)L.nchunks);
+                     a.topk_idx, a.k, max_len, (int)L.nchunks, nq);
   }
   const size_t smem = sizeof(uint64_t) * kCandCap + kBitmapTokens / 8 + sizeof(int) * L.nchunks;
   static size_t configured[64] = {0};
@@ -891,12 +892,12 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
   }
   cudaError_t e = launch_ex(k_topk_threshold, grid, dim3(kTopkThreads), smem, s, true, false,
                             a.seq_lens, scores, L.ld, w, a.topk_idx, a.k, max_len,
-                            (int)L.nchunks);
+                            (int)L.nchunks, nq);
   if (e != cudaSuccess || max_len <= kBitmapTokens) return e;
   return launch_ex(k_topk_emit, grid, dim3(kTopkThreads), 0, s, true, false, a.seq_lens,
                    reinterpret_cast<const uint32_t*>(ws + L.bits),
                    reinterpret_cast<const int32_t*>(ws + L.chunk_off), a.topk_idx, a.k, max_len,
-                   (int)L.nchunks);
+                   (int)L.nchunks, nq);
 }
 
 int topk_kernel_launches(const pks_decode_args& a, const WorkspaceLayout& L) {

@@ -49,7 +49,12 @@ pks_status check_shapes(const pks_decode_args* a) {
     return PKS_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return PKS_ERR_INVALID;
   if (a->topk_mode < 0 || a->topk_mode > 1) return PKS_ERR_INVALID;
-  if (a->reserved[0] || a->reserved[1]) return PKS_ERR_INVALID;
+  if (a->reserved[0]) return PKS_ERR_INVALID;
+  if (a->n_queries < 0) return PKS_ERR_INVALID;
+  // compiled: Nq in {1, 2, 4, 8} with Hi * Nq <= 8
+  const int nq = query_count(*a);
+  if ((nq & (nq - 1)) != 0 || (int64_t)a->Hi * nq > 8) return PKS_ERR_UNSUPPORTED;
+  if ((int64_t)a->B * query_count(*a) > kMaxB) return PKS_ERR_UNSUPPORTED;
   if ((int64_t)a->num_pages * a->page_size > INT32_MAX) return PKS_ERR_UNSUPPORTED;
   if (a->D != 64 && a->D != 128) return PKS_ERR_UNSUPPORTED;
   if (a->Di != 64 && a->Di != 128) return PKS_ERR_UNSUPPORTED;
@@ -93,7 +98,7 @@ pks_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKS_OK : PKS_ERR
 
 WorkspaceLayout workspace_layout(const pks_decode_args& a) {
   WorkspaceLayout L{};
-  const int64_t B = a.B;
+  const int64_t B = (int64_t)a.B * query_count(a);  // one virtual request per query token
   const int G = a.Hq / a.Hkv;
   const int64_t max_len = (int64_t)a.max_pages * a.page_size;
   L.nchunks = (int)std::max<int64_t>(1, (max_len + kTopkChunk - 1) / kTopkChunk);

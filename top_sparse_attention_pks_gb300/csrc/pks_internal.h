@@ -107,6 +107,11 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(const pks_decode_args& a);
 
+// Query tokens per request (n_queries 0 means one).  Top-k, attention and
+// merge run over B * Nq virtual requests, virtual request v = b * Nq + q
+// using request b's length and block table row.
+inline int query_count(const pks_decode_args& a) { return a.n_queries > 1 ? a.n_queries : 1; }
+
 // ---- kernel launchers (each returns cudaGetLastError() after launch) ----
 cudaError_t launch_indexer_scan(const pks_decode_args& a, int32_t* scores, int64_t ld,
                                 int32_t* hist, int32_t* err, cudaStream_t s);

@@ -19,12 +19,12 @@ class SparseDecodeStep:
                  stream=None):
         t = dict(tensors)
         q = t["q"]
-        B, Hq, D = q.shape
         dev = q.device
         self.tensors = t
         self.k = int(k)
-        self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
-        self.topk_idx = torch.empty((B, self.k), dtype=torch.int32, device=dev)
+        # q: [B, Hq, D], or [B, Nq, Hq, D] with Nq query tokens per request
+        self.out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        self.topk_idx = torch.empty(tuple(q.shape[:-2]) + (self.k,), dtype=torch.int32, device=dev)
         probe = pks.make_args(k=self.k, topk_idx=self.topk_idx, out=self.out,
                               attn_splits=attn_splits, topk_mode=topk_mode, **t)
         nbytes = pks.pks_decode_workspace_size(probe)
@@ -47,7 +47,7 @@ class SparseDecodeStep:
         pks.pks_sparse_attention(self.args, stream)
 
     def scores(self, stream=None) -> torch.Tensor:
-        B = self.args.B
+        B = self.args.B * max(1, self.args.n_queries)  # one row per query token
         ld = self.args.max_pages * self.args.page_size
         out = torch.zeros((B, ld), dtype=torch.int32, device=self.out.device)
         pks.pks_indexer_scores(self.args, out, stream)

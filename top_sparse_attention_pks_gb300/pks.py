@@ -48,7 +48,7 @@ class pks_decode_args(ctypes.Structure):
         ("topk_idx", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("attn_splits", ctypes.c_int32), ("topk_mode", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("n_queries", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1),
     ]
 
 
@@ -256,10 +256,20 @@ class Pool:
 def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: int,
               topk_idx=None, out=None, workspace=None, attn_splits: int = 0,
               topk_mode: int = 0, num_pages: Optional[int] = None) -> pks_decode_args:
-    """Fill a ``pks_decode_args`` from tensors (shapes are read off the tensors)."""
+    """Fill a ``pks_decode_args`` from tensors (shapes are read off the tensors).
+
+    ``q`` is [B, Hq, D], or [B, Nq, Hq, D] for Nq query tokens per request (then
+    ``q_idx`` is [B, Nq, Hi, Di], ``topk_idx`` [B, Nq, k], ``out`` [B, Nq, Hq, D])."""
     a = pks_decode_args()
-    B, Hq, D = q.shape
-    _, Hi, Di = q_idx.shape
+    if q.dim() == 4:
+        B, Nq, Hq, D = q.shape
+        if q_idx.dim() != 4 or q_idx.shape[:2] != q.shape[:2]:
+            raise ValueError("q_idx must be [B, Nq, Hi, Di] like q")
+        _, _, Hi, Di = q_idx.shape
+        a.n_queries = int(Nq)
+    else:
+        B, Hq, D = q.shape
+        _, Hi, Di = q_idx.shape
     npages, P, Hkv, D2 = kv_k.shape
     if D2 != D or tuple(kv_v.shape) != tuple(kv_k.shape):
         raise ValueError("kv_k / kv_v / q shapes disagree")
