@@ -349,7 +349,7 @@ static pks_status decode_impl(const pks_decode_args* args, pks_stream stream,
   if (st != PKS_OK) return st;
   if ((st = pks::check_common_ptrs(args)) != PKS_OK) return st;
   if ((st = pks::check_scan_ptrs(args)) != PKS_OK) return st;
-  if (!args->topk_idx) return PKS_ERR_INVALID;
+  if (args->B > 0 && !args->topk_idx) return PKS_ERR_INVALID;
   if (attention && (st = pks::check_attn_ptrs(args)) != PKS_OK) return st;
   const WorkspaceLayout L = pks::workspace_layout(*args);
   if ((st = pks::check_workspace(args, L)) != PKS_OK) return st;
