@@ -129,7 +129,8 @@ WorkspaceLayout workspace_layout(const pks_decode_args& a) {
   L.chunk_cnt = take(sizeof(int32_t) * 2 * (size_t)B * L.nchunks);
   L.chunk_off = take(sizeof(int32_t) * (size_t)B * L.nchunks);
   L.thresh = take(sizeof(TopkThreshold) * (size_t)B);
-  L.attn_prefix = take(sizeof(int32_t) * (size_t)(B + 1));
+  // position prefix over requests, then the attention grid for the merge
+  L.attn_prefix = take(sizeof(int32_t) * (size_t)(B + 2));
   // partial (m, l, o) slots: one per (CTA, segment) pair, indexed cta + segment
   const size_t nslots = (size_t)(L.attn_grid_max + nseg) * hg * G;
   L.part_ml = take(sizeof(float) * 2 * nslots);
