@@ -82,6 +82,9 @@ def _declare(L):
     L.orc_sparse_attention.argtypes = [_I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P,
                                        _P, _P, _P]
     L.orc_sparse_attention.restype = ctypes.c_int
+    L.orc_mla_sparse_attention.argtypes = [_I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
+                                           _P, _P, ctypes.c_double, _P]
+    L.orc_mla_sparse_attention.restype = ctypes.c_int
     L.orc_residency_init.argtypes = [_I32, _I32, _I32, _P, _P, _P, _P, _P]
     L.orc_residency_init.restype = ctypes.c_int
     L.orc_residency_step.argtypes = [_I32, _I32, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P,
@@ -204,6 +207,25 @@ def sparse_attention(block_table, page_size, idx, q, kv_k, kv_v):
     _check(lib().orc_sparse_attention(B, _ptr(bt), bt.shape[1], int(page_size), Hq, Hkv, D,
                                       ix.shape[1], _ptr(ix), _ptr(qa), _ptr(ka), _ptr(va),
                                       _ptr(out)), "sparse_attention")
+    return out
+
+
+def mla_sparse_attention(block_table, page_size, idx, q, kv, d, scale=None):
+    """Sparse MLA in MQA mode: q [B, H, d + r], kv pool [num_pages, page_size, d + r]
+    (bf16); scale defaults to 1 / sqrt(d + r).  double [B, H, d]."""
+    bt = _arr(block_table, np.int32)
+    ix = _arr(idx, np.int32)
+    qa = _arr(q, np.uint16)
+    ka = _arr(kv, np.uint16)
+    B, H, dk = qa.shape
+    assert ka.shape[-1] == dk and 0 < d <= dk
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    out = np.empty((B, H, d), dtype=np.float64)
+    _check(lib().orc_mla_sparse_attention(B, _ptr(bt), bt.shape[1], int(page_size), H, int(d),
+                                          dk - int(d), ix.shape[1], _ptr(ix), _ptr(qa),
+                                          _ptr(ka), float(scale), _ptr(out)),
+           "mla_sparse_attention")
     return out
 
 

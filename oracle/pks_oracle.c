@@ -256,6 +256,52 @@ int orc_sparse_attention(int32_t B, const int32_t* block_table, int32_t max_page
   return 0;
 }
 
+/* ------------------------------------------------- MLA in MQA mode (DSA) */
+
+int orc_mla_sparse_attention(int32_t B, const int32_t* block_table, int32_t max_pages,
+                             int32_t page_size, int32_t H, int32_t d, int32_t r, int32_t k,
+                             const int32_t* idx, const uint16_t* q, const uint16_t* kv,
+                             double scale, double* out) {
+  if (B < 0 || H <= 0 || d <= 0 || r < 0 || k <= 0 || !(scale > 0.0)) return -3;
+  const int32_t dk = d + r; /* key width: latent plus RoPE part */
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t h = 0; h < H; ++h) {
+      const uint16_t* qh = q + ((int64_t)b * H + h) * dk;
+      double* o = out + ((int64_t)b * H + h) * d;
+      for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
+      double* logit = (double*)malloc(sizeof(double) * (size_t)k);
+      int64_t* row = (int64_t*)malloc(sizeof(int64_t) * (size_t)k);
+      int32_t n = 0;
+      double m = -INFINITY;
+      for (int32_t j = 0; j < k; ++j) {
+        const int32_t t = idx[(int64_t)b * k + j];
+        if (t < 0) continue;
+        /* [SA] MQA mode: one latent row per token, shared by every query head */
+        const int64_t base = phys_token(block_table, max_pages, page_size, b, t) * dk;
+        double dot = 0.0;
+        for (int32_t c = 0; c < dk; ++c) dot += bf16_to_double(qh[c]) * bf16_to_double(kv[base + c]);
+        logit[n] = dot * scale;
+        row[n] = base;
+        if (logit[n] > m) m = logit[n];
+        ++n;
+      }
+      if (n > 0) {
+        double l = 0.0;
+        for (int32_t j = 0; j < n; ++j) l += exp(logit[j] - m);
+        for (int32_t j = 0; j < n; ++j) {
+          const double p = exp(logit[j] - m) / l;
+          /* [SA] the value is the latent part only (the first d of the d + r) */
+          for (int32_t c = 0; c < d; ++c) o[c] += p * bf16_to_double(kv[row[j] + c]);
+        }
+      }
+      free(logit);
+      free(row);
+    }
+  }
+  return 0;
+}
+
 /* -------------------------------------------------------------- residency */
 
 int orc_residency_init(int32_t num_pages, int32_t capacity, int32_t n_init,

@@ -91,6 +91,19 @@ int orc_sparse_attention(int32_t B, const int32_t* block_table, int32_t max_page
                          const int32_t* idx, const uint16_t* q, const uint16_t* kv_k,
                          const uint16_t* kv_v, double* out);
 
+/* [SA] DeepSeek Sparse Attention: the sparse MLA runs in MQA mode.  Every
+ *  token holds one latent row of d + r values (latent part d, RoPE part r),
+ *  shared by all H query heads; the key is the whole row, the value its first
+ *  d values:
+ *    o[b,h] = sum_j softmax_j(scale * q[b,h] . kv_j) kv_j[0:d],
+ *  j over the tokens idx[b, :] >= 0, kv_j = kv[phys(b, t_j)] read through the
+ *  block table from the pool [num_pages, page_size, d + r].  q: [B, H, d + r].
+ *  A request with no selected token gets o = 0.  out: double [B, H, d]. */
+int orc_mla_sparse_attention(int32_t B, const int32_t* block_table, int32_t max_pages,
+                             int32_t page_size, int32_t H, int32_t d, int32_t r, int32_t k,
+                             const int32_t* idx, const uint16_t* q, const uint16_t* kv,
+                             double scale, double* out);
+
 /* Residency table ([SA] HiSparse: LRU cache of KV pages in HBM, pages loaded on
  *  a top-k miss, evicted by least recent use).  State (caller arrays):
  *  page_slot [num_pages] (-1 = not resident), slot_page [capacity] (-1 = empty),
