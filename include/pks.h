@@ -320,6 +320,62 @@ pks_status pks_sparse_attention_resident(const pks_decode_args* args, const void
                                          int32_t capacity, const void* slot_k,
                                          const void* slot_v, pks_stream stream);
 
+/* ----------------------------------------------------------------------
+ * Sparse MLA in MQA mode ("Sparse Attention on GLM5.3 and HBM", DeepSeek
+ * Sparse Attention paragraphs: the sparse MLA of DSA runs in MQA mode; the
+ * pages' configuration is latent d = 512, RoPE r = 64, H = 64 or 128 query
+ * heads, 2-byte values).  Every token keeps one latent row of d + r values
+ * shared by all H heads:
+ *   out[b,h] = sum_j softmax_j(sm_scale * q[b,h] . kv_j) kv_j[0:d]
+ * j over the positions of topk_idx[b, :] holding a token (>= 0), kv_j the
+ * row of token t_j found through the block table.  The pages do not give the
+ * softmax scale: sm_scale 0 means 1 / sqrt(d + r).
+ * ---------------------------------------------------------------------- */
+typedef struct pks_mla_args {
+  int32_t B;              /* requests, 0..4096 */
+  int32_t H;              /* query heads, 1..128 */
+  int32_t d_latent;       /* d: must be 512 */
+  int32_t d_rope;         /* r: must be 64 */
+  int32_t page_size, max_pages, num_pages;
+  int32_t k;              /* entries per request in topk_idx, 1..65536 */
+  const int32_t* seq_lens;     /* device int32 [B] */
+  const int32_t* block_table;  /* device int32 [B, max_pages] */
+  const int32_t* topk_idx;     /* device int32 [B, k]: token positions, -1 = none */
+  const void* q;               /* device bf16 [B, H, d + r], 16-byte aligned */
+  const void* kv;              /* device bf16 [num_pages, page_size, d + r], 16-byte aligned */
+  void* out;                   /* device bf16 [B, H, d], 16-byte aligned (written) */
+  void* workspace;             /* device scratch owned by the caller, 256-byte aligned */
+  size_t workspace_bytes;
+  float sm_scale;              /* softmax scale; 0 = 1 / sqrt(d + r) */
+  int32_t trim;                /* 1: each list holds its selected entries first and -1
+                                  after (the decode step's own top-k), so only the first
+                                  min(k, len_b) positions are visited; 0: all k */
+  int32_t splits;              /* CTA pairs per request: 0 = automatic (one pair per two
+                                  SMs spread over the requests), else 1..64 */
+  int32_t reserved[1];         /* must be 0 */
+} pks_mla_args;
+
+/* Workspace bytes pks_mla_sparse_attention needs for these shapes (pointers
+ * may be NULL): a 16-byte device error word plus, with more than one split,
+ * the (m, l) and fp32 output partials of every (request, split, head). */
+pks_status pks_mla_workspace_size(const pks_mla_args* args, size_t* bytes);
+
+/* Sparse MLA over the selected tokens, asynchronous on the stream.  One CTA
+ * per (request, split, half of d) on the tcgen05 tensor cores (accumulators in
+ * tensor memory), 230 KB of shared memory each, plus one merge launch when
+ * splits > 1.  INVALID for NULL pointers (B > 0), misaligned pointers or
+ * shapes outside the ranges above; UNSUPPORTED for d != 512 or r != 64;
+ * WORKSPACE when the workspace is missing, misaligned or too small.  Device
+ * checks (page id, token position, length out of range) skip the token and
+ * set the workspace's error word, read by pks_mla_device_error.  The caller
+ * zeroes the error word once (pks_mla_device_error clears it). */
+pks_status pks_mla_sparse_attention(const pks_mla_args* args, pks_stream stream);
+
+/* Copy the MLA workspace's device error word to *code and clear it (codes as
+ * for pks_decode_device_error; 5: a bounded wait inside the kernel gave up).
+ * Synchronises the stream. */
+pks_status pks_mla_device_error(const pks_mla_args* args, int32_t* code, pks_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

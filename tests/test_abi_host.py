@@ -206,3 +206,34 @@ def test_residency_layout_on_host():
     assert n >= off["lru_order"] + 4 * 16384
     with pytest.raises(pks.PksError):
         pks.pks_residency_state_bytes(0, 4)
+
+
+def _mla_cpu_args(**over):
+    import ctypes
+    a = pks.pks_mla_args()
+    a.B, a.H, a.d_latent, a.d_rope = 16, 128, 512, 64
+    a.page_size, a.max_pages, a.num_pages, a.k = 64, 2048, 32768, 2048
+    for key, v in over.items():
+        setattr(a, key, v)
+    return a
+
+
+def test_mla_workspace_and_validation_without_gpu():
+    import ctypes
+    L = pks.lib()
+    n = ctypes.c_size_t()
+    assert L.pks_mla_workspace_size(ctypes.byref(_mla_cpu_args(splits=1)), ctypes.byref(n)) == 0
+    one = n.value
+    assert L.pks_mla_workspace_size(ctypes.byref(_mla_cpu_args(splits=4)), ctypes.byref(n)) == 0
+    # four splits: (m, l) and 512 fp32 partial values per (request, split, head)
+    assert n.value >= one + 16 * 4 * 128 * (8 + 512 * 4)
+    # no workspace -> PKS_ERR_WORKSPACE, before any device work
+    assert L.pks_mla_sparse_attention(ctypes.byref(_mla_cpu_args(B=0, splits=2)), None) == -7
+    for c in [dict(H=0), dict(H=129), dict(k=0), dict(B=-1), dict(splits=65), dict(trim=2),
+              dict(sm_scale=-1.0), dict(reserved=(ctypes.c_int32 * 1)(3)), dict(page_size=0)]:
+        assert L.pks_mla_workspace_size(ctypes.byref(_mla_cpu_args(**c)), ctypes.byref(n)) == -1, c
+    for c in [dict(d_latent=256), dict(d_rope=32)]:
+        assert L.pks_mla_workspace_size(ctypes.byref(_mla_cpu_args(**c)), ctypes.byref(n)) == -6, c
+    # null device pointers with B > 0
+    a = _mla_cpu_args()
+    assert L.pks_mla_sparse_attention(ctypes.byref(a), None) == -1

@@ -1,0 +1,546 @@
+// Sparse MLA decode in MQA mode on the fifth-generation tensor cores.
+//
+// "Sparse Attention on GLM5.3 and HBM", DeepSeek Sparse Attention paragraphs:
+// the sparse MLA runs in MQA mode.  Every token keeps one latent row of d + r
+// values (d = 512 latent, r = 64 RoPE) shared by all H query heads; a head's
+// scores use the whole row and its output is the softmax-weighted sum of the
+// latent part.  The pages' intensity model, 2H(2d + r) FLOP per (d + r) * 2
+// bytes, is about 1.89 H FLOP/B: with 64-128 heads both products are real
+// dense contractions with the heads as the M dimension, which is what the
+// tcgen05 MMA with its accumulator in tensor memory is for.
+//
+// One CTA per (request, split of its selected tokens, half of the latent
+// value width).  The 128 threads are the 128 rows of the MMA (query heads,
+// zero rows above H); thread i owns tensor-memory lane i.  Per 32-token tile:
+//   S[128 x 32]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
+//   P             = exp2(S * scale - m)         one thread per head row
+//   O[128 x 256] += P[128 x 32] . V[32 x 256]   tcgen05.mma, fp32 in TMEM
+// Tensor memory holds O (256 columns, this CTA's half of the value width) and
+// S (32 columns); all of O would fill it, hence the two halves, which both
+// compute S.  Q stays in shared memory for the whole CTA (144 KiB, 128-byte
+// swizzled, K-major); K/V tiles are gathered through the block table with
+// cp.async into a two-stage ring, and the same tile is the K operand
+// (K-major) and the V operand (MN-major).  P goes through shared memory
+// (64-byte swizzled, K-major).  The running max moves only when a tile's max
+// exceeds it by more than 8 (log2 units), so O is rarely rescaled in TMEM.
+// With several splits per request the CTAs write (m, l, O) partials that
+// k_mla_merge combines.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pks_internal.h"
+
+namespace pks {
+namespace {
+
+constexpr int kDL = kMlaLatent;             // latent width d (the value)
+constexpr int kDK = kMlaLatent + kMlaRope;  // key width d + r
+constexpr int kTile = 32;                   // tokens per tile (MMA N of S)
+constexpr int kRows = 128;                  // MMA M: query heads, zero padded
+constexpr int kHalf = kDL / 2;              // value columns per CTA
+constexpr int kNT = 128;
+constexpr int kBlk = kDK / 64;              // 64-value (128-byte) column blocks
+constexpr uint32_t kQBlockBytes = kRows * 128;
+constexpr uint32_t kKBlockBytes = kTile * 128;
+constexpr uint32_t kQBytes = kBlk * kQBlockBytes;
+constexpr uint32_t kKStageBytes = kBlk * kKBlockBytes;
+constexpr uint32_t kPBytes = kRows * kTile * 2;
+constexpr uint32_t kSmemBytes = kQBytes + 2 * kKStageBytes + kPBytes + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0, kTmemS = kHalf;
+constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
+
+static_assert(kDK % 64 == 0 && kDL % 64 == 0, "latent and key widths in 64-value blocks");
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void flag_error(int32_t* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// generic-proxy writes of this thread to shared memory become visible to the
+// tensor core's (async proxy) reads
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// ---- mbarrier (completion of committed MMAs) ------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait for the phase with the given parity; false when it gave up
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+// ---- tcgen05: tensor memory, MMA, commit ----------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem], bf16 inputs, fp32 accumulator
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive once on bar when every MMA this thread issued so far has completed
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's lane (warp w reads lanes
+// 32w .. 32w + 31); the wait is inside the same statement so no use of the
+// values can be scheduled before it
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};\n"
+      "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+// Shared-memory operand descriptor: start address, leading and stride byte
+// offsets (16-byte units), descriptor version 1, swizzle mode in bits 61-63
+// (2: 128-byte swizzle, 4: 64-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
+}
+constexpr uint32_t kSw128 = 2, kSw64 = 4;
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16
+// A and B (bits 7-9, 10-12 = 1), B major-ness in bit 16 (1: MN-major), N / 8
+// in bits 17-22, M / 16 in bits 24-28; A is K-major.
+constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t kIdescS = idesc_bf16(kRows, kTile, false);   // S = Q . K^T
+constexpr uint32_t kIdescO = idesc_bf16(kRows, kHalf, true);    // O += P . V
+
+__global__ void __launch_bounds__(kNT, 1)
+k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
+                const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
+                const int32_t* __restrict__ topk, float2* __restrict__ part_ml,
+                float* __restrict__ part_o, __nv_bfloat16* __restrict__ out,
+                int32_t* __restrict__ err, int B, int H, int page_size, int max_pages,
+                int num_pages, int k, int trim, int splits, float scale_log2) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_s, bar_o;
+  __shared__ uint32_t s_tmem;
+  __shared__ int32_t s_row[3][kTile];
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int half = blockIdx.x & 1;
+  const int split = (blockIdx.x >> 1) % splits;
+  const int b = (blockIdx.x >> 1) / splits;
+  if (b >= B) return;
+  const float kNegInf = __int_as_float(0xff800000);
+
+  const int max_len = max_pages * page_size;
+  int len = seq_lens[b];
+  if (len < 0 || len > max_len) {
+    if (tid == 0) flag_error(err, kErrLen);
+    len = -1;
+  }
+  // positions of the request's list to visit: its own top-k list holds the
+  // selected entries first (trim: min(k, len) of them), any other list is
+  // visited in full
+  const int npos = len < 0 ? 0 : (trim ? min(len, k) : k);
+  const int ntiles_req = (npos + kTile - 1) / kTile;
+  const int t_lo = (int)((int64_t)split * ntiles_req / splits);
+  const int t_hi = (int)((int64_t)(split + 1) * ntiles_req / splits);
+  const int ntiles = t_hi - t_lo;
+  const int64_t slot = (int64_t)b * splits + split;  // partial slot of this CTA
+  const int h = tid;                                   // this thread's head row
+
+  if (ntiles == 0) {  // nothing selected in this range
+    if (splits > 1) {
+      if (half == 0 && h < H) part_ml[slot * H + h] = make_float2(kNegInf, 0.f);
+    } else if (h < H) {
+      __nv_bfloat16* ob = out + ((int64_t)b * H + h) * kDL + half * kHalf;
+      for (int c = 0; c < kHalf; ++c) ob[c] = __float2bfloat16(0.f);
+    }
+    return;
+  }
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = base, sK = base + kQBytes, sP = sK + 2 * kKStageBytes;
+
+  // physical row of each position of tile `tile` (-1: none), threads 0..31
+  auto resolve = [&](int tile, int rs) {
+    if (tid >= kTile) return;
+    const int p = tile * kTile + tid;
+    int row = -1;
+    if (tile < t_hi && p < npos) {
+      const int t = topk[(int64_t)b * k + p];
+      if (t >= 0) {
+        if (t >= len) {
+          flag_error(err, kErrToken);
+        } else {
+          const int page = block_table[(int64_t)b * max_pages + t / page_size];
+          if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
+          else flag_error(err, kErrPage);
+        }
+      }
+    }
+    s_row[rs][tid] = row;
+  };
+  // gather a tile's 32 rows (576 values each) into stage `st`, 128-byte
+  // swizzle: 16-byte chunk c of row r in block j sits at chunk c ^ (r & 7)
+  auto load_tile = [&](int rs, int st) {
+    const uint32_t dst0 = sK + (uint32_t)st * kKStageBytes;
+    for (int id = tid; id < kTile * kBlk * 8; id += kNT) {
+      const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
+      const int j = cc >> 3, c = cc & 7;
+      const int row = s_row[rs][r];
+      const __nv_bfloat16* src = kv + (row >= 0 ? (int64_t)row * kDK + cc * 8 : 0);
+      cp_async16(dst0 + j * kKBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src, row >= 0 ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
+  if (tid == 32) {
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_o, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (tid == 0) s_abort = 0;
+  resolve(t_lo, 0);
+  resolve(t_lo + 1, 1);
+  // Q rows (heads; zero rows from H to 128), 128-byte swizzled K-major
+  {
+    const __nv_bfloat16* qb = q + (int64_t)b * H * kDK;
+    for (int id = tid; id < kRows * kBlk * 8; id += kNT) {
+      const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
+      const int j = cc >> 3, c = cc & 7;
+      const __nv_bfloat16* src = qb + (r < H ? (int64_t)r * kDK + cc * 8 : 0);
+      cp_async16(sQ + j * kQBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src, r < H ? 16 : 0);
+    }
+    cp_async_commit();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+  load_tile(0, 0);
+
+  float m_run = kNegInf, l_run = 0.f;
+  uint32_t ph_s = 0, ph_o = 0;
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t & 1, rs = t % 3;
+    cp_async_wait_all();
+    fence_async_smem();
+    __syncthreads();
+    if (s_abort) break;
+    // ---- S = Q . K^T over the 9 column blocks, 4 k-steps of 16 each
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t kst = sK + (uint32_t)st * kKStageBytes;
+#pragma unroll 1
+      for (int kk = 0; kk < kDK / 16; ++kk) {
+        const uint32_t off = (uint32_t)(kk & 3) * 32;  // k-step inside the 128-byte row
+        const uint64_t da = smem_desc(sQ + (kk >> 2) * kQBlockBytes + off, 16, 1024, kSw128);
+        const uint64_t db = smem_desc(kst + (kk >> 2) * kKBlockBytes + off, 16, 1024, kSw128);
+        mma_bf16(tmem + kTmemS, da, db, kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&bar_s);
+    }
+    // ---- the previous tile's O update has read its stage and P: refill
+    if (t > 0) {
+      if (!mbar_wait(&bar_o, ph_o)) ok = false;
+      ph_o ^= 1;
+      tc_fence_after();
+    }
+    if (t + 1 < ntiles) load_tile((t + 1) % 3, st ^ 1);
+    resolve(t_lo + t + 2, (t + 2) % 3);
+
+    // ---- softmax of this thread's head row over the tile
+    if (!mbar_wait(&bar_s, ph_s)) ok = false;
+    ph_s ^= 1;
+    tc_fence_after();
+    float sv[32];
+    tmem_ld32(tmem + lane_off + kTmemS, sv);
+    float mt = kNegInf;
+#pragma unroll
+    for (int j = 0; j < kTile; ++j) {
+      sv[j] = s_row[rs][j] >= 0 ? sv[j] * scale_log2 : kNegInf;
+      mt = fmaxf(mt, sv[j]);
+    }
+    const bool move = mt > m_run + 8.f;  // also true on the first valid tile
+    const float m_new = move ? mt : m_run;
+    const float alpha = move ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
+    float psum = 0.f;
+    uint32_t pk[kTile / 2];
+#pragma unroll
+    for (int j = 0; j < kTile; j += 2) {
+      const float p0 = sv[j] == kNegInf ? 0.f : exp2f(sv[j] - m_new);
+      const float p1 = sv[j + 1] == kNegInf ? 0.f : exp2f(sv[j + 1] - m_new);
+      const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+      psum += __low2float(pp) + __high2float(pp);
+      pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pp);
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+    // rescale the O accumulated so far (warp-wide: TMEM access is collective)
+    if (__any_sync(0xffffffffu, move && t > 0)) {
+      const float a = (move && t > 0) ? alpha : 1.f;
+#pragma unroll 1
+      for (int c = 0; c < kHalf / 32; ++c) {
+        float ov[32];
+        tmem_ld32(tmem + lane_off + kTmemO + c * 32, ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] *= a;
+        tmem_st32(tmem + lane_off + kTmemO + c * 32, ov);
+      }
+    }
+    // P row h: 32 bf16 = four 16-byte chunks, 64-byte swizzle (chunk c of
+    // row h at chunk c ^ ((h >> 1) & 3))
+    {
+      const uint32_t prow = sP + (uint32_t)h * 64;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t dst = prow + ((c ^ ((h >> 1) & 3)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(pk[4 * c]),
+                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                     : "memory");
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    if (!ok) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    // ---- O += P . V: V is this CTA's half of the tile's latent columns
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t vst = sK + (uint32_t)st * kKStageBytes + (uint32_t)half * (kHalf / 64) * kKBlockBytes;
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint64_t da = smem_desc(sP + kk * 32, 16, 512, kSw64);
+        const uint64_t db = smem_desc(vst + kk * 2048, kKBlockBytes, 1024, kSw128);
+        mma_bf16(tmem + kTmemO, da, db, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&bar_o);
+    }
+  }
+  cp_async_wait_all();
+
+  const bool aborted = s_abort != 0;
+  if (!aborted) {
+    if (!mbar_wait(&bar_o, ph_o)) {
+      flag_error(err, kErrTimeout);
+    } else {
+      tc_fence_after();
+      // ---- O of this CTA's half: to the output, or to the partial slot
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < kHalf / 32; ++c) {
+        float ov[32];
+        tmem_ld32(tmem + lane_off + kTmemO + c * 32, ov);
+        if (h < H) {
+          if (splits == 1) {
+            __nv_bfloat16* ob = out + ((int64_t)b * H + h) * kDL + half * kHalf + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w;
+              __nv_bfloat162 p0 = __floats2bfloat162_rn(ov[i] * inv, ov[i + 1] * inv);
+              __nv_bfloat162 p1 = __floats2bfloat162_rn(ov[i + 2] * inv, ov[i + 3] * inv);
+              __nv_bfloat162 p2 = __floats2bfloat162_rn(ov[i + 4] * inv, ov[i + 5] * inv);
+              __nv_bfloat162 p3 = __floats2bfloat162_rn(ov[i + 6] * inv, ov[i + 7] * inv);
+              w.x = *reinterpret_cast<uint32_t*>(&p0);
+              w.y = *reinterpret_cast<uint32_t*>(&p1);
+              w.z = *reinterpret_cast<uint32_t*>(&p2);
+              w.w = *reinterpret_cast<uint32_t*>(&p3);
+              *reinterpret_cast<uint4*>(ob + i) = w;
+            }
+          } else {
+            float* po = part_o + (slot * H + h) * kDL + half * kHalf + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(po + i) = make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+          }
+        }
+      }
+      if (splits > 1 && half == 0 && h < H) part_ml[slot * H + h] = make_float2(m_run, l_run);
+    }
+  } else if (tid == 0) {
+    flag_error(err, kErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// out[b, h] from the splits' partials: softmax-weighted by exp2(m_s - M)
+__global__ void __launch_bounds__(128)
+k_mla_merge(const float2* __restrict__ part_ml, const float* __restrict__ part_o,
+            __nv_bfloat16* __restrict__ out, int H, int splits) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const float kNegInf = __int_as_float(0xff800000);
+  float M = kNegInf;
+  for (int s = 0; s < splits; ++s) {
+    const float2 e = part_ml[((int64_t)b * splits + s) * H + h];
+    if (e.y > 0.f) M = fmaxf(M, e.x);
+  }
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < splits; ++s) {
+    const int64_t sl = ((int64_t)b * splits + s) * H + h;
+    const float2 e = part_ml[sl];
+    if (!(e.y > 0.f)) continue;
+    const float w = exp2f(e.x - M);
+    L += w * e.y;
+    const float4 v = reinterpret_cast<const float4*>(part_o + sl * kDL)[threadIdx.x];
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* ob = out + ((int64_t)b * H + h) * kDL + threadIdx.x * 4;
+  *reinterpret_cast<__nv_bfloat162*>(ob) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  *reinterpret_cast<__nv_bfloat162*>(ob + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+}
+
+}  // namespace
+
+int mla_splits(const pks_mla_args& a) {
+  if (a.splits > 0) return a.splits;
+  const int tiles = (a.k + kTile - 1) / kTile;
+  const int per = a.B > 0 ? device_sm_count() / (2 * a.B) : 1;
+  int s = per < 1 ? 1 : per;
+  if (s > tiles) s = tiles;
+  return s < 1 ? 1 : s;
+}
+
+MlaLayout mla_layout(const pks_mla_args& a) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  MlaLayout L{};
+  L.splits = mla_splits(a);
+  size_t off = 0;
+  L.err = off;
+  off = up(off + 16);
+  const size_t nslot = (size_t)a.B * (size_t)L.splits * (size_t)a.H;
+  L.part_ml = off;
+  off = up(off + (L.splits > 1 ? sizeof(float2) * nslot : 0));
+  L.part_o = off;
+  off = up(off + (L.splits > 1 ? sizeof(float) * nslot * kDL : 0));
+  L.total = off;
+  return L;
+}
+
+cudaError_t launch_mla(const pks_mla_args& a, const MlaLayout& L, cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!configured[dev & 63]) {
+    e = cudaFuncSetAttribute(k_mla_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev & 63] = true;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const float scale = a.sm_scale > 0.f ? a.sm_scale : 1.f / sqrtf((float)kDK);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const int grid = a.B * L.splits * 2;
+  k_mla_attention<<<grid, kNT, kSmemBytes, s>>>(
+      a.seq_lens, a.block_table, static_cast<const __nv_bfloat16*>(a.q),
+      static_cast<const __nv_bfloat16*>(a.kv), a.topk_idx,
+      reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
+      static_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.B, a.H,
+      a.page_size, a.max_pages, a.num_pages, a.k, a.trim ? 1 : 0, L.splits, scale_log2);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || L.splits == 1) return e;
+  k_mla_merge<<<dim3(a.H, a.B), 128, 0, s>>>(reinterpret_cast<const float2*>(ws + L.part_ml),
+                                             reinterpret_cast<const float*>(ws + L.part_o),
+                                             static_cast<__nv_bfloat16*>(a.out), a.H, L.splits);
+  return cudaGetLastError();
+}
+
+}  // namespace pks

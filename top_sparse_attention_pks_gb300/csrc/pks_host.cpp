@@ -621,4 +621,69 @@ pks_status pks_residency_fetch(const void* state, int32_t num_pages, int32_t cap
       capacity, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------ sparse MLA ---
+
+namespace {
+pks_status mla_check(const pks_mla_args* a) {
+  if (!a) return PKS_ERR_INVALID;
+  if (a->B < 0 || a->B > pks::kMaxB || a->H < 1 || a->H > 128 || a->page_size < 1 ||
+      a->max_pages < 1 || a->num_pages < 1 || a->k < 1 || a->k > pks::kMaxK ||
+      a->splits < 0 || a->splits > pks::kMlaMaxSplits || a->trim < 0 || a->trim > 1 ||
+      a->reserved[0] != 0 || !(a->sm_scale >= 0.f))
+    return PKS_ERR_INVALID;
+  if (a->d_latent != pks::kMlaLatent || a->d_rope != pks::kMlaRope) return PKS_ERR_UNSUPPORTED;
+  if ((int64_t)a->num_pages * a->page_size > INT32_MAX) return PKS_ERR_UNSUPPORTED;
+  if ((int64_t)a->max_pages * a->page_size > pks::kMaxLen) return PKS_ERR_UNSUPPORTED;
+  return PKS_OK;
+}
+pks_status mla_check_workspace(const pks_mla_args* a, const pks::MlaLayout& L) {
+  if (!a->workspace) return PKS_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & (pks::kAlign - 1)) != 0)
+    return PKS_ERR_WORKSPACE;
+  if (a->workspace_bytes < L.total) return PKS_ERR_WORKSPACE;
+  return PKS_OK;
+}
+}  // namespace
+
+pks_status pks_mla_workspace_size(const pks_mla_args* args, size_t* bytes) {
+  if (!bytes) return PKS_ERR_INVALID;
+  pks_status st = mla_check(args);
+  if (st != PKS_OK) return st;
+  *bytes = pks::mla_layout(*args).total;
+  return PKS_OK;
+}
+
+pks_status pks_mla_sparse_attention(const pks_mla_args* args, pks_stream stream) {
+  pks_status st = mla_check(args);
+  if (st != PKS_OK) return st;
+  if (args->B > 0) {
+    if (!args->seq_lens || !args->block_table || !args->topk_idx || !args->q || !args->kv ||
+        !args->out)
+      return PKS_ERR_INVALID;
+    if (!pks::aligned16(args->q) || !pks::aligned16(args->kv) || !pks::aligned16(args->out))
+      return PKS_ERR_INVALID;
+  }
+  const pks::MlaLayout L = pks::mla_layout(*args);
+  if ((st = mla_check_workspace(args, L)) != PKS_OK) return st;
+  if (args->B == 0) return PKS_OK;
+  return pks::from_cuda(pks::launch_mla(*args, L, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pks_status pks_mla_device_error(const pks_mla_args* args, int32_t* code, pks_stream stream) {
+  if (!code) return PKS_ERR_INVALID;
+  pks_status st = mla_check(args);
+  if (st != PKS_OK) return st;
+  const pks::MlaLayout L = pks::mla_layout(*args);
+  if ((st = mla_check_workspace(args, L)) != PKS_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* dev = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(args->workspace) + L.err);
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, dev, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dev, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return PKS_ERR_CUDA;
+  *code = host;
+  return PKS_OK;
+}
+
 }  // extern "C"

@@ -142,6 +142,17 @@ cudaError_t launch_residency_fetch(const int32_t* page_slot, const int32_t* miss
                                    const uint8_t* host_v, uint8_t* slot_k, uint8_t* slot_v,
                                    int64_t page_bytes, int num_pages, int capacity,
                                    cudaStream_t s);
+// ---- sparse MLA in MQA mode (tcgen05 kernel in k_mla.cu)
+constexpr int kMlaLatent = 512;  // d: latent width, the value
+constexpr int kMlaRope = 64;     // r: RoPE part of the key
+constexpr int kMlaMaxSplits = 64;
+struct MlaLayout {
+  int splits;
+  size_t err, part_ml, part_o, total;
+};
+int mla_splits(const pks_mla_args& a);
+MlaLayout mla_layout(const pks_mla_args& a);
+cudaError_t launch_mla(const pks_mla_args& a, const MlaLayout& L, cudaStream_t s);
 cudaError_t launch_residency(int32_t* state, int32_t num_pages, int32_t capacity, int32_t B,
                              int32_t k, int32_t page_size, int32_t max_pages,
                              const int32_t* topk_idx, const int32_t* block_table,

@@ -102,3 +102,81 @@ class ResidentDecodeStep:
         pks.pks_sparse_attention_resident(self.args, self.table.state, self.capacity, self.slot_k,
                                           self.slot_v, stream)
         return self.step.out, self.step.topk_idx
+
+
+class MlaAttention:
+    """Sparse MLA in MQA mode over given selections: ``pks_mla_sparse_attention``
+    with its own output and workspace.  q [B, H, d + r], kv [num_pages, P, d + r]
+    (bf16), topk_idx [B, k] (int32), d = 512 latent values."""
+
+    def __init__(self, seq_lens, block_table, topk_idx, q, kv, sm_scale: float = 0.0,
+                 trim: bool = False, splits: int = 0, stream=None):
+        dev = q.device
+        self.out = torch.empty((q.shape[0], q.shape[1], 512), dtype=torch.bfloat16, device=dev)
+        probe = pks.make_mla_args(seq_lens=seq_lens, block_table=block_table, topk_idx=topk_idx,
+                                  q=q, kv=kv, out=self.out, sm_scale=sm_scale, trim=trim,
+                                  splits=splits)
+        nbytes = pks.pks_mla_workspace_size(probe)
+        self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.args = pks.make_mla_args(seq_lens=seq_lens, block_table=block_table,
+                                      topk_idx=topk_idx, q=q, kv=kv, out=self.out,
+                                      workspace=self.workspace, sm_scale=sm_scale, trim=trim,
+                                      splits=splits)
+        self._keep = (seq_lens, block_table, topk_idx, q, kv)
+
+    def __call__(self, stream=None):
+        pks.pks_mla_sparse_attention(self.args, stream)
+        return self.out
+
+    def device_error(self, stream=None) -> int:
+        return pks.pks_mla_device_error(self.args, stream)
+
+
+class MlaDecodeStep:
+    """The DSA decode step with MLA attention: indexer scan and top-k
+    (``pks_decode_select``), then the sparse MLA over the selected tokens.
+    ``tensors``: seq_lens, block_table, q_idx, w_idx, idx_k as for the GQA
+    step, plus q [B, H, d + r] and kv [num_pages, P, d + r] (bf16)."""
+
+    def __init__(self, tensors: dict, k: int, topk_mode: int = 0, splits: int = 0,
+                 sm_scale: float = 0.0, stream=None):
+        t = dict(tensors)
+        q, kv = t["q"], t["kv"]
+        dev = q.device
+        B = q.shape[0]
+        self.k = int(k)
+        self.topk_idx = torch.empty((B, self.k), dtype=torch.int32, device=dev)
+        # selection arguments: the indexer and top-k fields of pks_decode_args
+        # (the GQA attention fields stay unset; select does not read them)
+        a = pks.pks_decode_args()
+        npages, P, _ = kv.shape
+        _, Hi, Di = t["q_idx"].shape
+        a.B, a.Hq, a.Hkv, a.D, a.Hi, a.Di = int(B), 1, 1, 64, int(Hi), int(Di)
+        a.page_size, a.max_pages = int(P), int(t["block_table"].shape[1])
+        a.num_pages, a.k = int(npages), self.k
+        a.seq_lens = pks._dptr(t["seq_lens"], torch.int32, "seq_lens")
+        a.block_table = pks._dptr(t["block_table"], torch.int32, "block_table")
+        a.q_idx = pks._dptr(t["q_idx"], torch.int8, "q_idx")
+        a.w_idx = pks._dptr(t["w_idx"], torch.int32, "w_idx")
+        a.idx_k = pks._dptr(t["idx_k"], torch.int8, "idx_k")
+        a.topk_idx = pks._dptr(self.topk_idx, torch.int32, "topk_idx")
+        a.topk_mode = int(topk_mode)
+        nbytes = pks.pks_decode_workspace_size(a)
+        self.select_workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        a.workspace = self.select_workspace.data_ptr()
+        a.workspace_bytes = self.select_workspace.numel()
+        pks.pks_decode_workspace_init(a, stream)
+        self.select_args = a
+        self.attention = MlaAttention(t["seq_lens"], t["block_table"], self.topk_idx, q, kv,
+                                      sm_scale=sm_scale, trim=True, splits=splits)
+        self.out = self.attention.out
+        self.tensors = t
+
+    def select(self, stream=None):
+        pks.pks_decode_select(self.select_args, stream)
+        return self.topk_idx
+
+    def __call__(self, stream=None):
+        pks.pks_decode_select(self.select_args, stream)
+        pks.pks_mla_sparse_attention(self.attention.args, stream)
+        return self.out, self.topk_idx

@@ -52,6 +52,19 @@ class pks_decode_args(ctypes.Structure):
     ]
 
 
+class pks_mla_args(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("d_latent", ctypes.c_int32),
+        ("d_rope", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("k", ctypes.c_int32),
+        ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+        ("topk_idx", ctypes.c_void_p), ("q", ctypes.c_void_p), ("kv", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t), ("sm_scale", ctypes.c_float),
+        ("trim", ctypes.c_int32), ("splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1),
+    ]
+
+
 def library_path() -> Path:
     return _LIB_PATH
 
@@ -125,6 +138,15 @@ def _declare(L):
     L.pks_residency_update.argtypes = [_P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P,
                                        _P]
     L.pks_residency_update.restype = _ST
+
+
+    _PM = ctypes.POINTER(pks_mla_args)
+    L.pks_mla_workspace_size.argtypes = [_PM, ctypes.POINTER(ctypes.c_size_t)]
+    L.pks_mla_workspace_size.restype = _ST
+    L.pks_mla_sparse_attention.argtypes = [_PM, _P]
+    L.pks_mla_sparse_attention.restype = _ST
+    L.pks_mla_device_error.argtypes = [_PM, ctypes.POINTER(ctypes.c_int32), _P]
+    L.pks_mla_device_error.restype = _ST
 
 
 def _check(code: int, where: str):
@@ -457,3 +479,54 @@ class ResidencyTable:
 
     def step_count(self) -> int:
         return int(self.state[:16].view(torch.int32)[2].item())
+
+
+# ---------------------------------------------------------------- sparse MLA
+
+
+def make_mla_args(*, seq_lens, block_table, topk_idx, q, kv, out=None, workspace=None,
+                  sm_scale: float = 0.0, trim: bool = False, splits: int = 0,
+                  d_latent: int = 512, num_pages: Optional[int] = None) -> pks_mla_args:
+    """Fill a ``pks_mla_args``: q [B, H, d + r], kv [num_pages, page_size, d + r],
+    topk_idx [B, k], out [B, H, d] (bf16 / int32 tensors on the device)."""
+    a = pks_mla_args()
+    B, H, dk = q.shape
+    npages, P, dk2 = kv.shape
+    if dk2 != dk or dk <= d_latent:
+        raise ValueError("q and kv must both be [..., d + r] with r > 0")
+    a.B, a.H, a.d_latent, a.d_rope = int(B), int(H), int(d_latent), int(dk - d_latent)
+    a.page_size, a.max_pages = int(P), int(block_table.shape[1])
+    a.num_pages = int(npages if num_pages is None else num_pages)
+    a.k = int(topk_idx.shape[-1])
+    a.seq_lens = _dptr(seq_lens, torch.int32, "seq_lens")
+    a.block_table = _dptr(block_table, torch.int32, "block_table")
+    a.topk_idx = _dptr(topk_idx, torch.int32, "topk_idx")
+    a.q = _dptr(q, torch.bfloat16, "q")
+    a.kv = _dptr(kv, torch.bfloat16, "kv")
+    a.out = _dptr(out, torch.bfloat16, "out")
+    if workspace is not None:
+        a.workspace = _dptr(workspace, torch.uint8, "workspace")
+        a.workspace_bytes = workspace.numel()
+    a.sm_scale = float(sm_scale)
+    a.trim = 1 if trim else 0
+    a.splits = int(splits)
+    return a
+
+
+def pks_mla_workspace_size(args: pks_mla_args) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().pks_mla_workspace_size(ctypes.byref(args), ctypes.byref(n)),
+           "pks_mla_workspace_size")
+    return n.value
+
+
+def pks_mla_sparse_attention(args: pks_mla_args, stream=None) -> None:
+    _check(lib().pks_mla_sparse_attention(ctypes.byref(args), _stream(stream)),
+           "pks_mla_sparse_attention")
+
+
+def pks_mla_device_error(args: pks_mla_args, stream=None) -> int:
+    code = ctypes.c_int32()
+    _check(lib().pks_mla_device_error(ctypes.byref(args), ctypes.byref(code), _stream(stream)),
+           "pks_mla_device_error")
+    return code.value

@@ -18,6 +18,15 @@ on GLM5.3 and HBM", HiSparse section; "Paged KV cache", worked example):
 * ``b256_8k_lru``     - 256 x 8192 tokens, HBM slot table holding half of the
   pages (LRU), compacted miss list per step.
 
+Three more follow the DeepSeek Sparse Attention paragraphs of the same page,
+whose sparse MLA runs in MQA mode (latent d = 512 plus RoPE r = 64 per token,
+one row shared by all query heads; H = 128 for DeepSeek V3.2, 64 for GLM-5).
+Their ``Hq`` is the MLA head count H, ``D`` the key width d + r, ``Hkv`` 1:
+
+* ``mla_paging_example`` - the worked example's five requests, H = 128, top-64.
+* ``mla_b16_128k``       - 16 x 131072 tokens, H = 128, top-2048.
+* ``mla_b64_32k_h64``    - 64 x 32768 tokens, H = 64, top-2048.
+
 Value distributions: K/V and attention queries are N(0, 1) rounded to bf16
 (round to nearest even); indexer queries and keys are integers uniform in
 [-127, 127]; indexer head weights are all one ("summed").
@@ -97,6 +106,21 @@ WORKLOADS = {
 #: the workloads in the order they are listed above
 WORKLOAD_ORDER = ["paging_example", "b32_4k", "b64_ragged_prefix", "b16_128k", "b256_8k_lru"]
 
+MLA_LATENT = 512  # d; the key width D of an MLA workload is d + r = 576
+
+MLA_WORKLOADS = {
+    "mla_paging_example": Workload(
+        name="mla_paging_example", B=5, seq_lens=(403, 96, 241, 30, 176), page_size=16,
+        Hq=128, Hkv=1, D=576, Hi=1, Di=64, k=64, num_pages=64, max_pages=32, seed=10),
+    "mla_b16_128k": Workload(
+        name="mla_b16_128k", B=16, seq_lens=(131072,) * 16, page_size=64, Hq=128, Hkv=1,
+        D=576, Hi=4, Di=128, k=2048, num_pages=32768, max_pages=2048, seed=13),
+    "mla_b64_32k_h64": Workload(
+        name="mla_b64_32k_h64", B=64, seq_lens=(32768,) * 64, page_size=64, Hq=64, Hkv=1,
+        D=576, Hi=1, Di=128, k=2048, num_pages=32768, max_pages=512, seed=14,
+        permute_pool=True),
+}
+
 
 def _gen(device, seed: int) -> torch.Generator:
     g = torch.Generator(device=device)
@@ -160,3 +184,19 @@ def draw_queries(wl: Workload, device="cpu", seed_offset: int = 0):
     q_idx = torch.randint(-127, 128, (wl.B, wl.Hi, wl.Di), generator=g, device=device,
                           dtype=torch.int8)
     return q, q_idx
+
+
+def draw_mla_tensors(wl: Workload, device="cpu", seed_offset: int = 0) -> dict:
+    """Large draws of an MLA workload on ``device``: ``q`` bf16 [B, H, d + r];
+    ``kv`` bf16 [num_pages, page_size, d + r] (one latent row per token);
+    ``q_idx`` int8 [B, Hi, Di]; ``w_idx`` int32 [Hi] (ones); ``idx_k`` int8
+    [num_pages, page_size, Di]."""
+    g = _gen(device, wl.seed * 1000003 + 7919 * seed_offset + 29)
+    P = wl.page_size
+    kv = torch.randn((wl.num_pages, P, wl.D), generator=g, device=device,
+                     dtype=torch.float32).to(torch.bfloat16)
+    idx_k = torch.randint(-127, 128, (wl.num_pages, P, wl.Di), generator=g, device=device,
+                          dtype=torch.int8)
+    q, q_idx = draw_queries(wl, device, seed_offset)
+    w_idx = torch.ones(wl.Hi, dtype=torch.int32, device=device)
+    return dict(q=q, q_idx=q_idx, w_idx=w_idx, kv=kv, idx_k=idx_k)
