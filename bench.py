@@ -33,8 +33,9 @@ sys.path.insert(0, str(ROOT))
 
 from top_sparse_attention_pks_gb300 import build as pkg_build  # noqa: E402
 from top_sparse_attention_pks_gb300 import pks  # noqa: E402
-from top_sparse_attention_pks_gb300.decoder import SparseDecodeStep  # noqa: E402
-from top_sparse_attention_pks_gb300.workloads import (WORKLOADS, draw_host,  # noqa: E402
+from top_sparse_attention_pks_gb300.decoder import MlaDecodeStep, SparseDecodeStep  # noqa: E402
+from top_sparse_attention_pks_gb300.workloads import (MLA_LATENT, MLA_WORKLOADS,  # noqa: E402
+                                                      WORKLOADS, draw_host, draw_mla_tensors,
                                                       draw_tensors)
 
 METRIC = "sparse decode steps/s"
@@ -222,7 +223,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="b16_128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="b16_128k",
+                    choices=sorted(WORKLOADS) + sorted(MLA_WORKLOADS))
     ap.add_argument("--impl", default="pks", choices=["pks", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-steps", type=int, default=200)
@@ -235,7 +237,15 @@ def main():
     ap.add_argument("--hisparse", action="store_true",
                     help="workloads with a slot table: K/V in pinned host memory, HBM slots, "
                          "misses fetched every step (select, update, fetch, attention)")
+    ap.add_argument("--mla", action="store_true",
+                    help="the DSA step with sparse MLA attention (MQA mode, tcgen05): "
+                         "indexer scan, top-k, MLA over the selection; default workload "
+                         "mla_b16_128k")
     args = ap.parse_args()
+    if args.mla and args.workload == "b16_128k":
+        args.workload = "mla_b16_128k"
+    if (args.workload in MLA_WORKLOADS) != args.mla:
+        ap.error("MLA workloads run with --mla (and --mla only with MLA workloads)")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
@@ -257,6 +267,11 @@ def main():
         pkg_build.build_library()
     if dist:
         dist.barrier()
+    if args.mla:
+        mla_bench(MLA_WORKLOADS[args.workload], args, dev, rank, world, dist)
+        if dist:
+            dist.destroy_process_group()
+        return
     wl = WORKLOADS[args.workload]
     if args.requests:
         wl = shrink(wl, args.requests)
@@ -443,6 +458,251 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def mla_setup(wl, device, seed_offset=0):
+    h = draw_host(wl)
+    pool = pks.Pool(wl.num_pages, wl.page_size, h["free_order"])
+    bt, _ = pool.build_block_table(h["seq_lens"], wl.max_pages, h["prefix_group"], wl.prefix_len)
+    pool.close()
+    t = draw_mla_tensors(wl, device, seed_offset)
+    t["seq_lens"] = h["seq_lens"].to(device)
+    t["block_table"] = torch.from_numpy(bt).to(device)
+    return t, h, bt
+
+
+def mla_algorithmic(wl, lens, bt, topk):
+    """One MLA step's algorithmic bytes and FLOPs: indexer keys scanned, the
+    unique selected latent rows (d + r bf16 values), queries and outputs; the
+    pages' MQA-mode FLOP count 2 H (d + r) + 2 H d per attended token."""
+    P = wl.page_size
+    scan_rows, kv_rows, attended = [], [], 0
+    for b, n in enumerate(lens):
+        n = int(n)
+        if n == 0:
+            continue
+        t = np.arange(n, dtype=np.int64)
+        scan_rows.append(bt[b, t // P].astype(np.int64) * P + t % P)
+        sel = topk[b][topk[b] >= 0].astype(np.int64)
+        kv_rows.append(bt[b, sel // P].astype(np.int64) * P + sel % P)
+        attended += sel.size
+    n_scan = np.unique(np.concatenate(scan_rows)).size if scan_rows else 0
+    n_kv = np.unique(np.concatenate(kv_rows)).size if kv_rows else 0
+    scan = n_scan * wl.Di
+    kv = n_kv * wl.D * 2
+    q = wl.B * wl.Hq * wl.D * 2
+    out = wl.B * wl.Hq * MLA_LATENT * 2
+    flops = attended * 2 * wl.Hq * (wl.D + MLA_LATENT)
+    return dict(scan=scan, kv=kv, q=q, out=out, attention=kv + q + out,
+                total=scan + kv + q + out, flops=flops, attended=attended)
+
+
+def time_mla_oracle(wl, t, budget_s, steps=None, warmup=0):
+    """The oracle's MLA step (indexer scores, top-k, MLA attention) on the
+    longest request, truncated so that a timed step fits the budget; the time
+    is scaled by tokens to the whole batch."""
+    import oracle
+    cores = oracle.set_threads(0)
+    lens = t["seq_lens"].cpu().numpy()
+    b = int(np.argmax(lens))
+    full = int(lens[b])
+    n_pages = -(-full // wl.page_size)
+    bt = t["block_table"].cpu().numpy()
+    pages = torch.from_numpy(bt[b, :n_pages].astype(np.int64)).to(t["kv"].device)
+    cbt = np.arange(n_pages, dtype=np.int32)[None]
+    q_idx = t["q_idx"].cpu().numpy()[b: b + 1]
+    w_idx = t["w_idx"].cpu().numpy()
+    q = t["q"].cpu()[b: b + 1]
+    idx_k = t["idx_k"].index_select(0, pages).cpu().numpy()
+    kv = t["kv"].index_select(0, pages).cpu()
+
+    def one(n_tok):
+        ln = np.array([n_tok], np.int32)
+        sc = oracle.indexer_scores(ln, cbt, wl.page_size, q_idx, w_idx, idx_k)
+        idx = oracle.topk(ln, sc, wl.k)
+        oracle.mla_sparse_attention(cbt, wl.page_size, idx, q, kv, MLA_LATENT)
+
+    n0 = min(full, max(4 * wl.k, 8192))
+    t0 = time.perf_counter()
+    one(n0)
+    c = (time.perf_counter() - t0) / n0
+    per_step = budget_s / max(1, (steps or 3) + warmup)
+    n_tok = int(min(full, max(min(full, 2 * wl.k), per_step / max(c, 1e-12))))
+    for _ in range(warmup):
+        one(n_tok)
+    times = []
+    for _ in range(steps or 3):
+        s0 = time.perf_counter()
+        one(n_tok)
+        times.append(time.perf_counter() - s0)
+    mean = sum(times) / len(times)
+    step_time = mean * float(lens.sum()) / n_tok
+    sample = (f"request {b} ({full} tokens) truncated to {n_tok} tokens per timed step, "
+              f"{len(times)} steps; time scaled by tokens to the {wl.B}-request batch")
+    return dict(value=1.0 / step_time, unit=UNIT, cores=cores, kind="oracle", sample=sample,
+                step_seconds=step_time)
+
+
+def mla_bench(wl, args, dev, rank, world, dist):
+    """The DSA decode step with sparse MLA: pks_decode_select (scan + top-k)
+    and pks_mla_sparse_attention, captured in one CUDA graph."""
+    if args.requests:
+        wl = shrink(wl, args.requests)
+    if args.topk:
+        wl = wl.replace(k=args.topk)
+    t, h, bt = mla_setup(wl, dev, seed_offset=rank)
+    cfg = config_dict(wl, args)
+    cfg.update({"attention": "sparse MLA, MQA mode (tcgen05)", "mla_heads": wl.Hq,
+                "latent_rope": [MLA_LATENT, wl.D - MLA_LATENT], "heads_q_kv": None,
+                "head_dim": None})
+    if args.impl == "reference":
+        ref = time_mla_oracle(wl, t, budget_s=120.0, steps=args.steps, warmup=args.warmup)
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": ref["value"],
+                          "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": ref["step_seconds"] * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "int64+f64", "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores",
+                                                               "kind", "sample")},
+                          "e2e": {"value": ref["value"], "unit": UNIT,
+                                  "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    step = MlaDecodeStep(t, wl.k)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            step(s)
+    torch.cuda.synchronize()
+    if step.attention.device_error(s) != 0:
+        raise RuntimeError("device-side check fired during warm-up")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    sel_launches = pks.pks_decode_launches(step.select_args) - 2  # scan + top-k only
+    # the MLA kernel, plus the merge when the workspace holds split partials
+    mla_launches = 1 + (1 if pks.pks_mla_workspace_size(step.attention.args) > 256 else 0)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush.zero_()
+            g.replay()
+    torch.cuda.synchronize()
+    ab = mla_algorithmic(wl, h["seq_lens"].numpy(), bt, step.topk_idx.cpu().numpy())
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index or 0)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(s):
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(s)
+            g.replay()
+            ends[i].record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    value, total_s = job_throughput(sum(step_ms) / 1e3, args.steps, world, dist, dev)
+    ms_per_step = total_s * 1e3 / args.steps
+
+    # stages: select (scan + top-k) and the MLA attention (+ merge), events on s
+    n_st = max(1, args.stage_steps)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_st)]
+    with torch.cuda.stream(s):
+        for row in evs:
+            for e in row:
+                e.record(s)
+        for i in range(n_st):
+            flush.zero_()
+            evs[i][0].record(s)
+            step.select(s)
+            evs[i][1].record(s)
+            pks.pks_mla_sparse_attention(step.attention.args, s)
+            evs[i][2].record(s)
+    torch.cuda.synchronize()
+    sel_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / n_st
+    mla_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / n_st
+    peak, peak_kind = measured_peaks()
+    peaks = json.loads((ROOT / "MEASURED_PEAKS.json").read_text()) if peak_kind == "measured" \
+        else {"bf16_tflops": 1900.0}
+    mla_gbs = ab["attention"] / (mla_ms * 1e-3) / 1e9
+    mla_tfs = ab["flops"] / (mla_ms * 1e-3) / 1e12
+    tf_peak = float(peaks["bf16_tflops"])
+    mla_roof = {"kernel": "k_mla_attention (+ k_mla_merge)", "launch_ms": mla_ms,
+                "algorithmic_bytes_per_launch": ab["attention"], "achieved_gbs": mla_gbs,
+                "frac_hbm": mla_gbs / peak, "flops_per_launch": ab["flops"],
+                "achieved_tflops": mla_tfs, "frac_bf16": mla_tfs / tf_peak,
+                "intensity_flop_per_byte": ab["flops"] / max(1, ab["attention"])}
+    if sel_ms >= mla_ms:
+        roofline = {"bound": "hbm", "kernel": "k_indexer_scan (+ top-k)",
+                    "achieved": ab["scan"] / (sel_ms * 1e-3) / 1e9, "peak": peak,
+                    "unit": "GB/s", "traffic": None, "algorithmic_bytes_per_launch": ab["scan"],
+                    "launch_ms": sel_ms}
+    else:
+        tensor = mla_roof["frac_bf16"] > mla_roof["frac_hbm"]
+        roofline = {"bound": "tensor" if tensor else "hbm", "kernel": "k_mla_attention",
+                    "achieved": mla_tfs if tensor else mla_gbs,
+                    "peak": tf_peak if tensor else peak,
+                    "unit": "TFLOP/s" if tensor else "GB/s", "traffic": None,
+                    "algorithmic_bytes_per_launch": ab["attention"], "launch_ms": mla_ms}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline["peak_kind"] = f"{peak_kind} (MEASURED_PEAKS.json)"
+
+    # end to end: queries and lengths/tables in from pinned host memory, the
+    # public calls, output and top-k back to pinned host memory
+    names = ["q", "q_idx", "seq_lens", "block_table"]
+    host_in = {n: t[n].cpu().pin_memory() for n in names}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    idx_h = torch.empty(step.topk_idx.shape, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = out_h.numel() * out_h.element_size() + idx_h.numel() * idx_h.element_size()
+    n = max(1, min(args.steps, args.e2e_steps))
+    tot = 0.0
+    with torch.cuda.stream(s):
+        for i in range(n + 3):
+            flush.zero_()
+            s.synchronize()
+            t0 = time.perf_counter()
+            for nm in names:
+                t[nm].copy_(host_in[nm], non_blocking=True)
+            pks.pks_decode_select(step.select_args, s)
+            pks.pks_mla_sparse_attention(step.attention.args, s)
+            out_h.copy_(step.out, non_blocking=True)
+            idx_h.copy_(step.topk_idx, non_blocking=True)
+            s.synchronize()
+            if i >= 3:
+                tot += time.perf_counter() - t0
+    e2e = {"value": n / tot, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": n, "timing": "host wall clock per step incl. copies and stream synchronise"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = time_mla_oracle(wl, t, budget_s=15.0)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        step_gbs = ab["total"] / (ms_per_step * 1e-3) / 1e9
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg, "roofline": roofline, "mla_attention": mla_roof,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": (sel_launches + mla_launches) * args.steps, "clocks": clk,
+            "step_hbm": {"algorithmic_bytes": ab["total"], "achieved_gbs": step_gbs,
+                         "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                         "frac_of_measured": step_gbs / peak},
+            "tokens_attended_per_s": ab["attended"] * value,
+            "stages_ms": {"select": sel_ms, "mla_attention": mla_ms},
+            "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+        }), flush=True)
 
 
 def hisparse_bench(wl, t, h, args, dev, rank):

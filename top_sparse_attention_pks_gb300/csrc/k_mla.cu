@@ -10,8 +10,9 @@
 // tcgen05 MMA with its accumulator in tensor memory is for.
 //
 // One CTA per (request, split of its selected tokens, half of the latent
-// value width).  The 128 threads are the 128 rows of the MMA (query heads,
-// zero rows above H); thread i owns tensor-memory lane i.  Per 32-token tile:
+// value width).  Threads 0-127 are the 128 rows of the MMA (query heads, zero
+// rows above H; thread i owns tensor-memory lane i); warp 4 is the producer.
+// Per 32-token tile:
 //   S[128 x 32]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
 //   P             = exp2(S * scale - m)         one thread per head row
 //   O[128 x 256] += P[128 x 32] . V[32 x 256]   tcgen05.mma, fp32 in TMEM
@@ -23,8 +24,18 @@
 // (K-major) and the V operand (MN-major).  P goes through shared memory
 // (64-byte swizzled, K-major).  The running max moves only when a tile's max
 // exceeds it by more than 8 (log2 units), so O is rarely rescaled in TMEM.
-// With several splits per request the CTAs write (m, l, O) partials that
-// k_mla_merge combines.
+//
+// Roles and hand-offs (mbarriers, every wait bounded):
+//   producer warp: resolves the rows of tile t + 2 through the block table
+//     (bar_rows), issues O += P.V of tile t - 1 once its P is written (bar_p,
+//     commit -> bar_o) and then S = Q.K^T of tile t once its gathers landed
+//     (bar_full, commit -> bar_s);
+//   softmax warps: after the O update of tile t - 1 (bar_o) gather tile t + 1
+//     into the freed stage, then take S of tile t (bar_s), write P, publish
+//     their gathers of tile t + 1 (bar_full) and P (bar_p).
+// So the tensor pipe runs O(t - 1) before S(t) and a stage is refilled while
+// the other one is being multiplied.  With several splits per request the
+// CTAs write (m, l, O) partials that k_mla_merge combines.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,7 +51,7 @@ constexpr int kDK = kMlaLatent + kMlaRope;  // key width d + r
 constexpr int kTile = 32;                   // tokens per tile (MMA N of S)
 constexpr int kRows = 128;                  // MMA M: query heads, zero padded
 constexpr int kHalf = kDL / 2;              // value columns per CTA
-constexpr int kNT = 128;
+constexpr int kThreads = kRows + 32;   // 4 softmax warps + the producer warp
 constexpr int kBlk = kDK / 64;              // 64-value (128-byte) column blocks
 constexpr uint32_t kQBlockBytes = kRows * 128;
 constexpr uint32_t kKBlockBytes = kTile * 128;
@@ -92,10 +103,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // bounded wait for the phase with the given parity; false when it gave up
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// or when another warp of the CTA has given up (*abort set)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (*abort || clock64() - t0 > kWaitCycles) return false;
   return true;
 }
 
@@ -175,6 +188,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
 // Shared-memory operand descriptor: start address, leading and stride byte
 // offsets (16-byte units), descriptor version 1, swizzle mode in bits 61-63
 // (2: 128-byte swizzle, 4: 64-byte swizzle).
@@ -195,7 +211,7 @@ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
 constexpr uint32_t kIdescS = idesc_bf16(kRows, kTile, false);   // S = Q . K^T
 constexpr uint32_t kIdescO = idesc_bf16(kRows, kHalf, true);    // O += P . V
 
-__global__ void __launch_bounds__(kNT, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                 const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
                 const int32_t* __restrict__ topk, float2* __restrict__ part_ml,
@@ -203,12 +219,15 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
                 int32_t* __restrict__ err, int B, int H, int page_size, int max_pages,
                 int num_pages, int k, int trim, int splits, float scale_log2) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_s, bar_o;
+  // bar_rows[i]: tile rows of slot i published (producer); bar_s: S ready;
+  // bar_p: P written (128 softmax threads); bar_o: O update done
+  __shared__ __align__(8) uint64_t bar_rows[2], bar_full[2], bar_s, bar_p, bar_o;
   __shared__ uint32_t s_tmem;
   __shared__ int32_t s_row[3][kTile];
+  __shared__ uint32_t s_mask[3];
   __shared__ int s_abort;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = blockIdx.x & 1;
   const int split = (blockIdx.x >> 1) % splits;
   const int b = (blockIdx.x >> 1) / splits;
@@ -230,14 +249,16 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   const int t_hi = (int)((int64_t)(split + 1) * ntiles_req / splits);
   const int ntiles = t_hi - t_lo;
   const int64_t slot = (int64_t)b * splits + split;  // partial slot of this CTA
-  const int h = tid;                                   // this thread's head row
+  const int h = tid;                                   // head row of a softmax thread
 
   if (ntiles == 0) {  // nothing selected in this range
-    if (splits > 1) {
-      if (half == 0 && h < H) part_ml[slot * H + h] = make_float2(kNegInf, 0.f);
-    } else if (h < H) {
-      __nv_bfloat16* ob = out + ((int64_t)b * H + h) * kDL + half * kHalf;
-      for (int c = 0; c < kHalf; ++c) ob[c] = __float2bfloat16(0.f);
+    if (h < H) {
+      if (splits > 1) {
+        if (half == 0) part_ml[slot * H + h] = make_float2(kNegInf, 0.f);
+      } else {
+        __nv_bfloat16* ob = out + ((int64_t)b * H + h) * kDL + half * kHalf;
+        for (int c = 0; c < kHalf; ++c) ob[c] = __float2bfloat16(0.f);
+      }
     }
     return;
   }
@@ -245,139 +266,226 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = base, sK = base + kQBytes, sP = sK + 2 * kKStageBytes;
 
-  // physical row of each position of tile `tile` (-1: none), threads 0..31
-  auto resolve = [&](int tile, int rs) {
-    if (tid >= kTile) return;
-    const int p = tile * kTile + tid;
-    int row = -1;
-    if (tile < t_hi && p < npos) {
-      const int t = topk[(int64_t)b * k + p];
-      if (t >= 0) {
-        if (t >= len) {
-          flag_error(err, kErrToken);
-        } else {
-          const int page = block_table[(int64_t)b * max_pages + t / page_size];
-          if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
-          else flag_error(err, kErrPage);
-        }
-      }
-    }
-    s_row[rs][tid] = row;
-  };
-  // gather a tile's 32 rows (576 values each) into stage `st`, 128-byte
-  // swizzle: 16-byte chunk c of row r in block j sits at chunk c ^ (r & 7)
-  auto load_tile = [&](int rs, int st) {
-    const uint32_t dst0 = sK + (uint32_t)st * kKStageBytes;
-    for (int id = tid; id < kTile * kBlk * 8; id += kNT) {
-      const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
-      const int j = cc >> 3, c = cc & 7;
-      const int row = s_row[rs][r];
-      const __nv_bfloat16* src = kv + (row >= 0 ? (int64_t)row * kDK + cc * 8 : 0);
-      cp_async16(dst0 + j * kKBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src, row >= 0 ? 16 : 0);
-    }
-    cp_async_commit();
-  };
-
   if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
-  if (tid == 32) {
+  if (tid == kRows) {
+    mbar_init(&bar_rows[0], 1);
+    mbar_init(&bar_rows[1], 1);
+    mbar_init(&bar_full[0], kRows);
+    mbar_init(&bar_full[1], kRows);
     mbar_init(&bar_s, 1);
+    mbar_init(&bar_p, kRows);
     mbar_init(&bar_o, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    s_abort = 0;
   }
-  if (tid == 0) s_abort = 0;
-  resolve(t_lo, 0);
-  resolve(t_lo + 1, 1);
-  // Q rows (heads; zero rows from H to 128), 128-byte swizzled K-major
+  // Q rows (heads; zero rows from H to 128), 128-byte swizzled K-major: 16-byte
+  // chunk c of row r in column block j sits at chunk c ^ (r & 7)
   {
     const __nv_bfloat16* qb = q + (int64_t)b * H * kDK;
-    for (int id = tid; id < kRows * kBlk * 8; id += kNT) {
+    for (int id = tid; id < kRows * kBlk * 8; id += kThreads) {
       const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
       const int j = cc >> 3, c = cc & 7;
       const __nv_bfloat16* src = qb + (r < H ? (int64_t)r * kDK + cc * 8 : 0);
       cp_async16(sQ + j * kQBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src, r < H ? 16 : 0);
     }
     cp_async_commit();
+    cp_async_wait_all();
+    fence_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
-  load_tile(0, 0);
 
-  float m_run = kNegInf, l_run = 0.f;
-  uint32_t ph_s = 0, ph_o = 0;
-  bool ok = true;
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t & 1, rs = t % 3;
-    cp_async_wait_all();
-    fence_async_smem();
-    __syncthreads();
-    if (s_abort) break;
-    // ---- S = Q . K^T over the 9 column blocks, 4 k-steps of 16 each
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t kst = sK + (uint32_t)st * kKStageBytes;
-#pragma unroll 1
-      for (int kk = 0; kk < kDK / 16; ++kk) {
-        const uint32_t off = (uint32_t)(kk & 3) * 32;  // k-step inside the 128-byte row
-        const uint64_t da = smem_desc(sQ + (kk >> 2) * kQBlockBytes + off, 16, 1024, kSw128);
-        const uint64_t db = smem_desc(kst + (kk >> 2) * kKBlockBytes + off, 16, 1024, kSw128);
-        mma_bf16(tmem + kTmemS, da, db, kIdescS, kk > 0 ? 1u : 0u);
+  if (warp == kRows / 32) {
+    // ================= producer warp: rows, K/V gathers, MMA issue =========
+    // physical row of each position of tile `tile` (-1: none); lane = position
+    auto resolve = [&](int tile, int rs) {
+      const int p = tile * kTile + lane;
+      int row = -1;
+      if (tile < t_hi && p < npos) {
+        const int t = topk[(int64_t)b * k + p];
+        if (t >= 0) {
+          if (t >= len) {
+            flag_error(err, kErrToken);
+          } else {
+            const int page = block_table[(int64_t)b * max_pages + t / page_size];
+            if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
+            else flag_error(err, kErrPage);
+          }
+        }
       }
-      mma_commit(&bar_s);
-    }
-    // ---- the previous tile's O update has read its stage and P: refill
-    if (t > 0) {
-      if (!mbar_wait(&bar_o, ph_o)) ok = false;
-      ph_o ^= 1;
-      tc_fence_after();
-    }
-    if (t + 1 < ntiles) load_tile((t + 1) % 3, st ^ 1);
-    resolve(t_lo + t + 2, (t + 2) % 3);
-
-    // ---- softmax of this thread's head row over the tile
-    if (!mbar_wait(&bar_s, ph_s)) ok = false;
-    ph_s ^= 1;
-    tc_fence_after();
-    float sv[32];
-    tmem_ld32(tmem + lane_off + kTmemS, sv);
-    float mt = kNegInf;
+      s_row[rs][lane] = row;
+      const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
+      if (lane == 0) s_mask[rs] = m;
+      __syncwarp();
+    };
+    const uint64_t dq0 = smem_desc(sQ, 16, 1024, kSw128);
+    const uint64_t dp0 = smem_desc(sP, 16, 512, kSw64);
+    auto issue_pv = [&](int tt) {  // O += P . V(tile tt)
+      const uint32_t vst = sK + (uint32_t)(tt & 1) * kKStageBytes +
+                           (uint32_t)half * (kHalf / 64) * kKBlockBytes;
+      const uint64_t dv0 = smem_desc(vst, kKBlockBytes, 1024, kSw128);
 #pragma unroll
-    for (int j = 0; j < kTile; ++j) {
-      sv[j] = s_row[rs][j] >= 0 ? sv[j] * scale_log2 : kNegInf;
-      mt = fmaxf(mt, sv[j]);
-    }
-    const bool move = mt > m_run + 8.f;  // also true on the first valid tile
-    const float m_new = move ? mt : m_run;
-    const float alpha = move ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
-    float psum = 0.f;
-    uint32_t pk[kTile / 2];
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16(tmem + kTmemO, dp0 + (uint64_t)((kk * 32) >> 4),
+                 dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO, (tt > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(&bar_o);
+    };
+    // lane 0 waits, the warp follows: control flow stays warp-uniform
+    auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
+      bool w = lane == 0 ? mbar_wait(bar, parity, &s_abort) : true;
+      __syncwarp();
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    };
+    bool ok = true;
+    // rows of the first two tiles; the softmax warps gather a tile once its
+    // rows are published on bar_rows
+    resolve(t_lo, 0);
+    if (lane == 0) mbar_arrive(&bar_rows[0]);
+    resolve(t_lo + 1, 1);
+    if (lane == 0) mbar_arrive(&bar_rows[1]);
+    for (int t = 0; t < ntiles && ok; ++t) {
+      // 1. the previous tile's O update, as soon as its P is written (it
+      //    also frees that tile's stage and the S accumulator)
+      if (t > 0) {
+        if (!wait0(&bar_p, (t - 1) & 1)) { ok = false; break; }
+        if (lane == 0) {
+          tc_fence_after();
+          issue_pv(t - 1);
+        }
+        __syncwarp();
+      }
+      // 2. S = Q . K^T of this tile once the softmax warps' gathers landed
+      if (!wait0(&bar_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t dk0 = smem_desc(sK + (uint32_t)(t & 1) * kKStageBytes, 16, 1024, kSw128);
 #pragma unroll
-    for (int j = 0; j < kTile; j += 2) {
-      const float p0 = sv[j] == kNegInf ? 0.f : exp2f(sv[j] - m_new);
-      const float p1 = sv[j + 1] == kNegInf ? 0.f : exp2f(sv[j + 1] - m_new);
-      const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-      psum += __low2float(pp) + __high2float(pp);
-      pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pp);
-    }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-    // rescale the O accumulated so far (warp-wide: TMEM access is collective)
-    if (__any_sync(0xffffffffu, move && t > 0)) {
-      const float a = (move && t > 0) ? alpha : 1.f;
-#pragma unroll 1
-      for (int c = 0; c < kHalf / 32; ++c) {
-        float ov[32];
-        tmem_ld32(tmem + lane_off + kTmemO + c * 32, ov);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] *= a;
-        tmem_st32(tmem + lane_off + kTmemO + c * 32, ov);
+        for (int kk = 0; kk < kDK / 16; ++kk)
+          mma_bf16(tmem + kTmemS,
+                   dq0 + (uint64_t)(((kk >> 2) * kQBlockBytes + (kk & 3) * 32) >> 4),
+                   dk0 + (uint64_t)(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4), kIdescS,
+                   kk > 0 ? 1u : 0u);
+        mma_commit(&bar_s);
+      }
+      __syncwarp();
+      // 3. rows of the tile after next (its slot was last read by the
+      //    softmax warps for tile t - 1, which have written its P)
+      if (t + 2 < ntiles) {
+        resolve(t_lo + t + 2, (t + 2) % 3);
+        if (lane == 0) mbar_arrive(&bar_rows[t & 1]);
       }
     }
-    // P row h: 32 bf16 = four 16-byte chunks, 64-byte swizzle (chunk c of
-    // row h at chunk c ^ ((h >> 1) & 3))
-    {
+    if (ok) {
+      if (!wait0(&bar_p, (ntiles - 1) & 1)) ok = false;
+      else if (lane == 0) {
+        tc_fence_after();
+        issue_pv(ntiles - 1);
+      }
+    }
+    if (!ok && lane == 0) {
+      flag_error(err, kErrTimeout);
+      s_abort = 1;
+    }
+  } else {
+    // ================= softmax warps: one thread per head row ==============
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+    // every lane waits; a vote keeps control flow warp-uniform (the TMEM
+    // accesses are warp-collective)
+    auto waitw = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &s_abort)) != 0;
+    };
+    float m_run = kNegInf, l_run = 0.f;
+    bool ok = true;
+    // gather tile `tile` into stage st: 32 rows x 72 16-byte chunks, 128-byte
+    // swizzle (chunk c of row r in column block j at chunk c ^ (r & 7))
+    auto load_tile = [&](int tile, int st) {
+      const int rs = tile % 3;
+      const uint32_t dst0 = sK + (uint32_t)st * kKStageBytes;
+#pragma unroll 2
+      for (int id = tid; id < kTile * kBlk * 8; id += kRows) {
+        const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
+        const int j = cc >> 3, c = cc & 7;
+        const int row = s_row[rs][r];
+        const __nv_bfloat16* src = kv + (row >= 0 ? (int64_t)row * kDK + cc * 8 : 0);
+        cp_async16(dst0 + j * kKBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src,
+                   row >= 0 ? 16 : 0);
+      }
+      cp_async_commit();
+    };
+    // this thread's gathers of a tile have landed: make them visible to the
+    // tensor core and count them on the stage's barrier
+    auto publish = [&](int st) {
+      cp_async_wait_all();
+      fence_async_smem();
+      mbar_arrive(&bar_full[st]);
+    };
+    if (!waitw(&bar_rows[0], 0)) ok = false;
+    if (ok) {
+      load_tile(0, 0);
+      publish(0);
+    }
+    for (int t = 0; t < ntiles && ok; ++t) {
+      // the O update of tile t - 1 has read its stage (the next tile's) and P
+      if (t > 0) {
+        if (!waitw(&bar_o, (t - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const bool next = t + 1 < ntiles;
+      if (next) {
+        if (!waitw(&bar_rows[(t + 1) & 1], ((t + 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        load_tile(t + 1, (t + 1) & 1);
+      }
+      if (!waitw(&bar_s, t & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t mask = s_mask[t % 3];
+      float sv[32];
+      tmem_ld32(tmem + lane_off + kTmemS, sv);
+      float mt = kNegInf;
+#pragma unroll
+      for (int j = 0; j < kTile; ++j) {
+        sv[j] = (mask >> j) & 1u ? sv[j] * scale_log2 : kNegInf;
+        mt = fmaxf(mt, sv[j]);
+      }
+      const bool move = mt > m_run + 8.f;  // also true on the first valid tile
+      const float m_new = move ? mt : m_run;
+      const float alpha = move ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
+      float psum = 0.f;
+      uint32_t pk[kTile / 2];
+#pragma unroll
+      for (int j = 0; j < kTile; j += 2) {
+        const float p0 = sv[j] == kNegInf ? 0.f : exp2f(sv[j] - m_new);
+        const float p1 = sv[j + 1] == kNegInf ? 0.f : exp2f(sv[j + 1] - m_new);
+        const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+        psum += __low2float(pp) + __high2float(pp);
+        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pp);
+      }
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      // rescale the O accumulated so far (warp-wide: TMEM access is collective)
+      if (__any_sync(0xffffffffu, move && t > 0)) {
+        const float a = (move && t > 0) ? alpha : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < kHalf / 32; ++c) {
+          float ov[32];
+          tmem_ld32(tmem + lane_off + kTmemO + c * 32, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] *= a;
+          tmem_st32(tmem + lane_off + kTmemO + c * 32, ov);
+        }
+      }
+      // P row h: 32 bf16 = four 16-byte chunks, 64-byte swizzle (chunk c of
+      // row h at chunk c ^ ((h >> 1) & 3))
       const uint32_t prow = sP + (uint32_t)h * 64;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -386,34 +494,14 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
                      "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
       }
+      fence_async_smem();
+      tc_fence_before();
+      if (next) publish((t + 1) & 1);
+      mbar_arrive(&bar_p);
     }
-    fence_async_smem();
-    tc_fence_before();
-    if (!ok) s_abort = 1;
-    __syncthreads();
-    if (s_abort) break;
-    // ---- O += P . V: V is this CTA's half of the tile's latent columns
-    if (tid == 0) {
+    // ---- O of this CTA's half: to the output, or to the partial slot
+    if (ok && waitw(&bar_o, (ntiles - 1) & 1)) {
       tc_fence_after();
-      const uint32_t vst = sK + (uint32_t)st * kKStageBytes + (uint32_t)half * (kHalf / 64) * kKBlockBytes;
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint64_t da = smem_desc(sP + kk * 32, 16, 512, kSw64);
-        const uint64_t db = smem_desc(vst + kk * 2048, kKBlockBytes, 1024, kSw128);
-        mma_bf16(tmem + kTmemO, da, db, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(&bar_o);
-    }
-  }
-  cp_async_wait_all();
-
-  const bool aborted = s_abort != 0;
-  if (!aborted) {
-    if (!mbar_wait(&bar_o, ph_o)) {
-      flag_error(err, kErrTimeout);
-    } else {
-      tc_fence_after();
-      // ---- O of this CTA's half: to the output, or to the partial slot
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
       for (int c = 0; c < kHalf / 32; ++c) {
@@ -439,14 +527,19 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
             float* po = part_o + (slot * H + h) * kDL + half * kHalf + c * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(po + i) = make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+              *reinterpret_cast<float4*>(po + i) =
+                  make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
           }
         }
       }
       if (splits > 1 && half == 0 && h < H) part_ml[slot * H + h] = make_float2(m_run, l_run);
+    } else {
+      ok = false;
     }
-  } else if (tid == 0) {
-    flag_error(err, kErrTimeout);
+    if (!ok && lane == 0) {
+      flag_error(err, kErrTimeout);
+      s_abort = 1;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -529,7 +622,7 @@ cudaError_t launch_mla(const pks_mla_args& a, const MlaLayout& L, cudaStream_t s
   const float scale = a.sm_scale > 0.f ? a.sm_scale : 1.f / sqrtf((float)kDK);
   const float scale_log2 = scale * 1.4426950408889634f;
   const int grid = a.B * L.splits * 2;
-  k_mla_attention<<<grid, kNT, kSmemBytes, s>>>(
+  k_mla_attention<<<grid, kThreads, kSmemBytes, s>>>(
       a.seq_lens, a.block_table, static_cast<const __nv_bfloat16*>(a.q),
       static_cast<const __nv_bfloat16*>(a.kv), a.topk_idx,
       reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
