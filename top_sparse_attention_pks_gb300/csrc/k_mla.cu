@@ -12,18 +12,22 @@
 // One CTA per (request, split of its selected tokens, half of the latent
 // value width).  Threads 0-127 are the 128 rows of the MMA (query heads, zero
 // rows above H; thread i owns tensor-memory lane i); warp 4 is the producer.
-// Per 32-token tile:
-//   S[128 x 32]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
+// Per 64-token tile:
+//   S[128 x 64]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
 //   P             = exp2(S * scale - m)         one thread per head row
-//   O[128 x 256] += P[128 x 32] . V[32 x 256]   tcgen05.mma, fp32 in TMEM
-// Tensor memory holds O (256 columns, this CTA's half of the value width) and
-// S (32 columns); all of O would fill it, hence the two halves, which both
-// compute S.  Q stays in shared memory for the whole CTA (144 KiB, 128-byte
-// swizzled, K-major); K/V tiles are gathered through the block table with
-// cp.async into a two-stage ring, and the same tile is the K operand
+//   O[128 x 256] += P[128 x 64] . V[64 x 256]   tcgen05.mma, fp32 in TMEM
+// A tcgen05.mma costs about the same time for N = 32 or 64 and M = 64 or
+// 128 (measured), so S is computed 64 tokens at a time.  Tensor memory holds
+// O (256 columns: this CTA's half of the value width; all of O would fill
+// it, hence the two halves, which both compute S), S (64 columns) and Q's
+// values 0..383 (192 columns, the A operand of 24 of the 36 k-steps of S);
+// Q's values 384..575 stay in shared memory (48 KiB, 128-byte swizzled,
+// K-major).  K/V tiles are gathered through the block table with cp.async
+// into a two-stage ring (72 KiB each); the same tile is the K operand
 // (K-major) and the V operand (MN-major).  P goes through shared memory
-// (64-byte swizzled, K-major).  The running max moves only when a tile's max
-// exceeds it by more than 8 (log2 units), so O is rarely rescaled in TMEM.
+// (128-byte swizzled, K-major).  The running max moves only when a tile's
+// max exceeds it by more than 8 (log2 units), so O is rarely rescaled in
+// TMEM.
 //
 // Roles and hand-offs (mbarriers, every wait bounded):
 //   producer warp: resolves the rows of tile t + 2 through the block table
@@ -48,19 +52,23 @@ namespace {
 
 constexpr int kDL = kMlaLatent;             // latent width d (the value)
 constexpr int kDK = kMlaLatent + kMlaRope;  // key width d + r
-constexpr int kTile = 32;                   // tokens per tile (MMA N of S)
+constexpr int kTile = 64;                   // tokens per tile (MMA N of S)
 constexpr int kRows = 128;                  // MMA M: query heads, zero padded
 constexpr int kHalf = kDL / 2;              // value columns per CTA
 constexpr int kThreads = kRows + 32;   // 4 softmax warps + the producer warp
 constexpr int kBlk = kDK / 64;              // 64-value (128-byte) column blocks
+constexpr int kQTmemDims = 384;             // Q values 0..383 live in tensor memory
+constexpr int kQSmemBlk = (kDK - kQTmemDims) / 64;  // the rest: 3 column blocks in smem
 constexpr uint32_t kQBlockBytes = kRows * 128;
 constexpr uint32_t kKBlockBytes = kTile * 128;
-constexpr uint32_t kQBytes = kBlk * kQBlockBytes;
+constexpr uint32_t kQBytes = kQSmemBlk * kQBlockBytes;
 constexpr uint32_t kKStageBytes = kBlk * kKBlockBytes;
-constexpr uint32_t kPBytes = kRows * kTile * 2;
+constexpr uint32_t kPBytes = kRows * kTile * 2;  // 128-byte rows
 constexpr uint32_t kSmemBytes = kQBytes + 2 * kKStageBytes + kPBytes + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0, kTmemS = kHalf;
+// tensor-memory columns: O (fp32), S (fp32), Q values 0..383 (two bf16 a column)
+constexpr uint32_t kTmemO = 0, kTmemS = kHalf, kTmemQ = kHalf + kTile;
+static_assert(kTmemQ + kQTmemDims / 2 == kTmemCols, "O, S and Q fill the tensor memory");
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 
 static_assert(kDK % 64 == 0 && kDL % 64 == 0, "latent and key widths in 64-value blocks");
@@ -131,6 +139,14 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
 
+// 2^x with the hardware's approximate exponential (ex2.approx: a few ulp in
+// fp32); the probabilities it gives are rounded to bf16 for the P.V product
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // D[tmem] (+)= A[smem] . B[smem], bf16 inputs, fp32 accumulator
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -138,6 +154,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] . B[smem]: A's rows in the D lanes, two bf16 a column
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // arrive once on bar when every MMA this thread issued so far has completed
@@ -199,7 +224,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
          ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
 }
-constexpr uint32_t kSw128 = 2, kSw64 = 4;
+constexpr uint32_t kSw128 = 2;
 
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16
 // A and B (bits 7-9, 10-12 = 1), B major-ness in bit 16 (1: MN-major), N / 8
@@ -224,7 +249,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   __shared__ __align__(8) uint64_t bar_rows[2], bar_full[2], bar_s, bar_p, bar_o;
   __shared__ uint32_t s_tmem;
   __shared__ int32_t s_row[3][kTile];
-  __shared__ uint32_t s_mask[3];
+  __shared__ uint32_t s_mask[3][kTile / 32];
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -278,15 +303,25 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     s_abort = 0;
   }
-  // Q rows (heads; zero rows from H to 128), 128-byte swizzled K-major: 16-byte
-  // chunk c of row r in column block j sits at chunk c ^ (r & 7)
+  // Q rows (heads; zero rows from H to 128).  Values 384..575: 128-byte
+  // swizzled K-major in shared memory (16-byte chunk c of row r in column
+  // block j at chunk c ^ (r & 7)).  Values 0..383: staged row by row in the
+  // K stages (rows padded to 784 bytes), then copied by each head's thread
+  // into its tensor-memory lane.
+  constexpr uint32_t kQStageRow = kQTmemDims * 2 + 16;
   {
     const __nv_bfloat16* qb = q + (int64_t)b * H * kDK;
     for (int id = tid; id < kRows * kBlk * 8; id += kThreads) {
       const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
-      const int j = cc >> 3, c = cc & 7;
       const __nv_bfloat16* src = qb + (r < H ? (int64_t)r * kDK + cc * 8 : 0);
-      cp_async16(sQ + j * kQBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src, r < H ? 16 : 0);
+      uint32_t dst;
+      if (cc < kQTmemDims / 8) {
+        dst = sK + r * kQStageRow + cc * 16;
+      } else {
+        const int j = (cc - kQTmemDims / 8) >> 3, c = cc & 7;
+        dst = sQ + j * kQBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
+      }
+      cp_async16(dst, src, r < H ? 16 : 0);
     }
     cp_async_commit();
     cp_async_wait_all();
@@ -296,32 +331,61 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  if (tid < kRows) {
+    const uint32_t lo = (uint32_t)(warp * 32) << 16;
+    const uint32_t src = sK + (uint32_t)tid * kQStageRow;
+#pragma unroll 1
+    for (int c = 0; c < kQTmemDims / 64; ++c) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                     : "r"(src + (uint32_t)(c * 128 + i * 4)));
+        v[i] = __uint_as_float(x0);
+        v[i + 1] = __uint_as_float(x1);
+        v[i + 2] = __uint_as_float(x2);
+        v[i + 3] = __uint_as_float(x3);
+      }
+      tmem_st32(tmem + lo + kTmemQ + c * 32, v);
+    }
+  }
+  // the staging area becomes the K stages: every thread is done reading it
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == kRows / 32) {
     // ================= producer warp: rows, K/V gathers, MMA issue =========
-    // physical row of each position of tile `tile` (-1: none); lane = position
+    // physical row of each position of tile `tile` (-1: none); lane handles
+    // positions lane and lane + 32
     auto resolve = [&](int tile, int rs) {
-      const int p = tile * kTile + lane;
-      int row = -1;
-      if (tile < t_hi && p < npos) {
-        const int t = topk[(int64_t)b * k + p];
-        if (t >= 0) {
-          if (t >= len) {
-            flag_error(err, kErrToken);
-          } else {
-            const int page = block_table[(int64_t)b * max_pages + t / page_size];
-            if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
-            else flag_error(err, kErrPage);
+#pragma unroll
+      for (int w = 0; w < kTile / 32; ++w) {
+        const int pos = w * 32 + lane;
+        const int p = tile * kTile + pos;
+        int row = -1;
+        if (tile < t_hi && p < npos) {
+          const int t = topk[(int64_t)b * k + p];
+          if (t >= 0) {
+            if (t >= len) {
+              flag_error(err, kErrToken);
+            } else {
+              const int page = block_table[(int64_t)b * max_pages + t / page_size];
+              if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
+              else flag_error(err, kErrPage);
+            }
           }
         }
+        s_row[rs][pos] = row;
+        const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
+        if (lane == 0) s_mask[rs][w] = m;
       }
-      s_row[rs][lane] = row;
-      const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
-      if (lane == 0) s_mask[rs] = m;
       __syncwarp();
     };
     const uint64_t dq0 = smem_desc(sQ, 16, 1024, kSw128);
-    const uint64_t dp0 = smem_desc(sP, 16, 512, kSw64);
+    const uint64_t dp0 = smem_desc(sP, 16, 1024, kSw128);
     auto issue_pv = [&](int tt) {  // O += P . V(tile tt)
       const uint32_t vst = sK + (uint32_t)(tt & 1) * kKStageBytes +
                            (uint32_t)half * (kHalf / 64) * kKBlockBytes;
@@ -329,7 +393,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk)
         mma_bf16(tmem + kTmemO, dp0 + (uint64_t)((kk * 32) >> 4),
-                 dv0 + (uint64_t)((kk * 2048) >> 4), kIdescO, (tt > 0 || kk > 0) ? 1u : 0u);
+                 dv0 + (uint64_t)((kk * 16 * 128) >> 4), kIdescO, (tt > 0 || kk > 0) ? 1u : 0u);
       mma_commit(&bar_o);
     };
     // lane 0 waits, the warp follows: control flow stays warp-uniform
@@ -362,11 +426,17 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         tc_fence_after();
         const uint64_t dk0 = smem_desc(sK + (uint32_t)(t & 1) * kKStageBytes, 16, 1024, kSw128);
 #pragma unroll
-        for (int kk = 0; kk < kDK / 16; ++kk)
-          mma_bf16(tmem + kTmemS,
-                   dq0 + (uint64_t)(((kk >> 2) * kQBlockBytes + (kk & 3) * 32) >> 4),
-                   dk0 + (uint64_t)(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4), kIdescS,
-                   kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kDK / 16; ++kk) {
+          const uint64_t db = dk0 + (uint64_t)(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4);
+          if (kk < kQTmemDims / 16) {
+            mma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + kk * 8, db, kIdescS, kk > 0 ? 1u : 0u);
+          } else {
+            const int qk = kk - kQTmemDims / 16;
+            mma_bf16(tmem + kTmemS,
+                     dq0 + (uint64_t)(((qk >> 2) * kQBlockBytes + (qk & 3) * 32) >> 4), db,
+                     kIdescS, 1u);
+          }
+        }
         mma_commit(&bar_s);
       }
       __syncwarp();
@@ -448,13 +518,15 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         break;
       }
       tc_fence_after();
-      const uint32_t mask = s_mask[t % 3];
-      float sv[32];
-      tmem_ld32(tmem + lane_off + kTmemS, sv);
+      const uint32_t mask0 = s_mask[t % 3][0], mask1 = s_mask[t % 3][1];
+      float sv[kTile];
+      tmem_ld32(tmem + lane_off + kTmemS, *reinterpret_cast<float(*)[32]>(&sv[0]));
+      tmem_ld32(tmem + lane_off + kTmemS + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
       float mt = kNegInf;
 #pragma unroll
       for (int j = 0; j < kTile; ++j) {
-        sv[j] = (mask >> j) & 1u ? sv[j] * scale_log2 : kNegInf;
+        const uint32_t mk = j < 32 ? mask0 : mask1;
+        sv[j] = (mk >> (j & 31)) & 1u ? sv[j] * scale_log2 : kNegInf;
         mt = fmaxf(mt, sv[j]);
       }
       const bool move = mt > m_run + 8.f;  // also true on the first valid tile
@@ -464,8 +536,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       uint32_t pk[kTile / 2];
 #pragma unroll
       for (int j = 0; j < kTile; j += 2) {
-        const float p0 = sv[j] == kNegInf ? 0.f : exp2f(sv[j] - m_new);
-        const float p1 = sv[j + 1] == kNegInf ? 0.f : exp2f(sv[j + 1] - m_new);
+        const float p0 = sv[j] == kNegInf ? 0.f : ex2_approx(sv[j] - m_new);
+        const float p1 = sv[j + 1] == kNegInf ? 0.f : ex2_approx(sv[j + 1] - m_new);
         const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
         psum += __low2float(pp) + __high2float(pp);
         pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pp);
@@ -484,12 +556,12 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
           tmem_st32(tmem + lane_off + kTmemO + c * 32, ov);
         }
       }
-      // P row h: 32 bf16 = four 16-byte chunks, 64-byte swizzle (chunk c of
-      // row h at chunk c ^ ((h >> 1) & 3))
-      const uint32_t prow = sP + (uint32_t)h * 64;
+      // P row h: 64 bf16 = eight 16-byte chunks, 128-byte swizzle (chunk c of
+      // row h at chunk c ^ (h & 7))
+      const uint32_t prow = sP + (uint32_t)h * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t dst = prow + ((c ^ ((h >> 1) & 3)) << 4);
+      for (int c = 0; c < kTile / 8; ++c) {
+        const uint32_t dst = prow + ((c ^ (h & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(pk[4 * c]),
                      "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
