@@ -646,12 +646,14 @@ def mla_bench(wl, args, dev, rank, world, dist):
                     "achieved": ab["scan"] / (sel_ms * 1e-3) / 1e9, "peak": peak,
                     "unit": "GB/s", "traffic": None, "algorithmic_bytes_per_launch": ab["scan"],
                     "launch_ms": sel_ms}
+    mla_roof["traffic"] = profiled_traffic("mla", wl.name)
     else:
         tensor = mla_roof["frac_bf16"] > mla_roof["frac_hbm"]
         roofline = {"bound": "tensor" if tensor else "hbm", "kernel": "k_mla_attention",
                     "achieved": mla_tfs if tensor else mla_gbs,
                     "peak": tf_peak if tensor else peak,
-                    "unit": "TFLOP/s" if tensor else "GB/s", "traffic": None,
+                    "unit": "TFLOP/s" if tensor else "GB/s",
+                    "traffic": profiled_traffic("mla", wl.name),
                     "algorithmic_bytes_per_launch": ab["attention"], "launch_ms": mla_ms}
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
     roofline["peak_kind"] = f"{peak_kind} (MEASURED_PEAKS.json)"
@@ -815,14 +817,19 @@ def config_dict(wl, args):
             "timing": "CUDA events around each CUDA-graph replay of the step"}
 
 
+PROFILED = {"scan": ("k_indexer.cu", "k_indexer_scan"),
+            "attention": ("k_attention.cu", "k_sparse_attention"),
+            "mla": ("k_mla.cu", "k_mla_attention")}
+
+
 def profiled_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
     import hashlib
-    src = ROOT / "top_sparse_attention_pks_gb300" / "csrc" / (
-        "k_indexer.cu" if kernel == "scan" else "k_attention.cu")
+    src_name, prof_name = PROFILED[kernel]
+    src = ROOT / "top_sparse_attention_pks_gb300" / "csrc" / src_name
     sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    prof = ROOT / "profiles" / f"{'k_indexer_scan' if kernel == 'scan' else 'k_sparse_attention'}_{workload}.md"
+    prof = ROOT / "profiles" / f"{prof_name}_{workload}.md"
     if not prof.exists():
         return None
     kv = {}
