@@ -641,12 +641,12 @@ def mla_bench(wl, args, dev, rank, world, dist):
                 "frac_hbm": mla_gbs / peak, "flops_per_launch": ab["flops"],
                 "achieved_tflops": mla_tfs, "frac_bf16": mla_tfs / tf_peak,
                 "intensity_flop_per_byte": ab["flops"] / max(1, ab["attention"])}
+    mla_roof["traffic"] = profiled_traffic("mla", wl.name)
     if sel_ms >= mla_ms:
         roofline = {"bound": "hbm", "kernel": "k_indexer_scan (+ top-k)",
                     "achieved": ab["scan"] / (sel_ms * 1e-3) / 1e9, "peak": peak,
                     "unit": "GB/s", "traffic": None, "algorithmic_bytes_per_launch": ab["scan"],
                     "launch_ms": sel_ms}
-    mla_roof["traffic"] = profiled_traffic("mla", wl.name)
     else:
         tensor = mla_roof["frac_bf16"] > mla_roof["frac_hbm"]
         roofline = {"bound": "tensor" if tensor else "hbm", "kernel": "k_mla_attention",
