@@ -44,7 +44,8 @@ def build(force: bool = False) -> Path:
                                                   (_HERE / "pks_oracle.h").stat().st_mtime)):
         return _LIB_PATH
     tmp = _LIB_PATH.with_suffix(f".{os.getpid()}.tmp")
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall", "-Wextra",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+           "-Wall", "-Wextra",
            "-o", str(tmp), str(_SRC), "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
@@ -82,6 +83,11 @@ def _declare(L):
     L.orc_sparse_attention.argtypes = [_I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P,
                                        _P, _P, _P]
     L.orc_sparse_attention.restype = ctypes.c_int
+    L.orc_indexer_scores_f.argtypes = [_I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P,
+                                       _I64]
+    L.orc_indexer_scores_f.restype = ctypes.c_int
+    L.orc_topk_f.argtypes = [_I32, _P, _P, _I64, _I32, _P]
+    L.orc_topk_f.restype = ctypes.c_int
     L.orc_mla_sparse_attention.argtypes = [_I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                            _P, _P, ctypes.c_double, _P]
     L.orc_mla_sparse_attention.restype = ctypes.c_int
@@ -181,6 +187,33 @@ def indexer_scores(seq_lens, block_table, page_size, q_idx, w_idx, idx_k, ld=Non
     _check(lib().orc_indexer_scores(B, _ptr(lens), _ptr(bt), max_pages, int(page_size), Hi, Di,
                                     _ptr(qi), _ptr(w), _ptr(ik), _ptr(out), int(ld)),
            "indexer_scores")
+    return out
+
+
+def indexer_scores_f(seq_lens, block_table, page_size, q_idx, w_f, idx_k, ld=None):
+    """Float-weighted indexer scores: float32 [B, ld] (fp32, heads in order)."""
+    lens = _arr(seq_lens, np.int32)
+    bt = _arr(block_table, np.int32)
+    qi = _arr(q_idx, np.int8)
+    wf = _arr(w_f, np.float32)
+    ik = _arr(idx_k, np.int8)
+    B, Hi, Di = qi.shape
+    assert wf.shape == (B, Hi)
+    if ld is None:
+        ld = int(bt.shape[1]) * int(page_size)
+    out = np.zeros((B, ld), dtype=np.float32)
+    _check(lib().orc_indexer_scores_f(B, _ptr(lens), _ptr(bt), bt.shape[1], int(page_size), Hi,
+                                      Di, _ptr(qi), _ptr(wf), _ptr(ik), _ptr(out), int(ld)),
+           "indexer_scores_f")
+    return out
+
+
+def topk_f(seq_lens, scores, k):
+    lens = _arr(seq_lens, np.int32)
+    sc = _arr(scores, np.float32)
+    B = lens.shape[0]
+    out = np.empty((B, k), dtype=np.int32)
+    _check(lib().orc_topk_f(B, _ptr(lens), _ptr(sc), sc.shape[1], int(k), _ptr(out)), "topk_f")
     return out
 
 

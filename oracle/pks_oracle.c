@@ -202,6 +202,74 @@ int orc_topk(int32_t B, const int32_t* lens, const int64_t* scores, int64_t ld, 
   return rc;
 }
 
+/* ------------------------------------------- indexer with real head weights */
+
+int orc_indexer_scores_f(int32_t B, const int32_t* lens, const int32_t* block_table,
+                         int32_t max_pages, int32_t page_size, int32_t Hi, int32_t Di,
+                         const int8_t* q_idx, const float* w_f, const int8_t* idx_k,
+                         float* scores, int64_t ld) {
+  if (B < 0 || Hi <= 0 || Di <= 0 || page_size <= 0) return -3;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t t = 0; t < lens[b]; ++t) {
+      const int8_t* key = idx_k + phys_token(block_table, max_pages, page_size, b, t) * Di;
+      /* [SA] weighted sum of the heads' ReLU logits, in fp32: heads in
+       * order, each product and each sum rounded to nearest on its own */
+      float s = 0.0f;
+      for (int32_t h = 0; h < Hi; ++h) {
+        const int8_t* qh = q_idx + ((int64_t)b * Hi + h) * Di;
+        int64_t dot = 0;
+        for (int32_t d = 0; d < Di; ++d) dot += (int64_t)qh[d] * (int64_t)key[d];
+        const float relu = (float)(dot > 0 ? dot : 0); /* exact: below 2^24 */
+        const float prod = w_f[(int64_t)b * Hi + h] * relu;
+        s = s + prod;
+      }
+      scores[(int64_t)b * ld + t] = s;
+    }
+  }
+  return 0;
+}
+
+typedef struct {
+  float score;
+  int32_t t;
+} fscored_token;
+
+static int by_fscore_desc_index_asc(const void* x, const void* y) {
+  const fscored_token* a = (const fscored_token*)x;
+  const fscored_token* b = (const fscored_token*)y;
+  if (a->score != b->score) return a->score > b->score ? -1 : 1;
+  return (a->t > b->t) - (a->t < b->t);
+}
+
+int orc_topk_f(int32_t B, const int32_t* lens, const float* scores, int64_t ld, int32_t k,
+               int32_t* idx) {
+  if (B < 0 || k <= 0) return -3;
+  int rc = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t* row = idx + (int64_t)b * k;
+    for (int32_t j = 0; j < k; ++j) row[j] = -1;
+    const int32_t len = lens[b];
+    if (len <= k) {
+      for (int32_t t = 0; t < len; ++t) row[t] = t; /* [SA] dense below K */
+      continue;
+    }
+    fscored_token* all = (fscored_token*)malloc(sizeof(fscored_token) * (size_t)len);
+    if (!all) { rc = -4; continue; }
+    for (int32_t t = 0; t < len; ++t) {
+      all[t].score = scores[(int64_t)b * ld + t];
+      all[t].t = t;
+    }
+    /* [SA] top-K by indexer score; equal scores (-0 equals +0) go to the lower index */
+    qsort(all, (size_t)len, sizeof(fscored_token), by_fscore_desc_index_asc);
+    for (int32_t j = 0; j < k; ++j) row[j] = all[j].t;
+    free(all);
+    qsort(row, (size_t)k, sizeof(int32_t), int32_asc);
+  }
+  return rc;
+}
+
 /* -------------------------------------------------------------- attention */
 
 static double bf16_to_double(uint16_t bits) {

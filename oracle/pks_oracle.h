@@ -81,6 +81,23 @@ int orc_indexer_scores(int32_t B, const int32_t* lens, const int32_t* block_tabl
 int orc_topk(int32_t B, const int32_t* lens, const int64_t* scores, int64_t ld, int32_t k,
              int32_t* idx);
 
+/* [SA] lightning indexer with real-valued head weights (the DSA form: a
+ *  weighted sum of the heads' ReLU logits).  w_f: float [B, Hi], per request.
+ *    s[b,t] = sum_h w_f[b,h] * max(0, q_idx[b,h,:] . k_idx[phys(b,t),:])
+ *  evaluated in fp32 with the heads in order 0..Hi-1, each product and each
+ *  sum rounded to nearest on its own (no fused multiply-add); the integer
+ *  dot products are exact and below 2^24, so their conversion is exact.
+ *  The pages fix no summation order: this order is the convention both sides
+ *  of the parity check follow.  Scores to scores[b*ld + t] (float). */
+int orc_indexer_scores_f(int32_t B, const int32_t* lens, const int32_t* block_table,
+                         int32_t max_pages, int32_t page_size, int32_t Hi, int32_t Di,
+                         const int8_t* q_idx, const float* w_f, const int8_t* idx_k,
+                         float* scores, int64_t ld);
+
+/* orc_topk on float scores: (score descending, token ascending), -0 == +0. */
+int orc_topk_f(int32_t B, const int32_t* lens, const float* scores, int64_t ld, int32_t k,
+               int32_t* idx);
+
 /* [SA] scaled dot-product attention over the selected tokens only:
  *    o[b,h] = sum_j softmax_j(q[b,h] . K_j / sqrt(D)) V_j,
  *  j over the tokens idx[b, :] >= 0, K_j / V_j read through the block table
