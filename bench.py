@@ -35,8 +35,8 @@ from top_sparse_attention_pks_gb300 import build as pkg_build  # noqa: E402
 from top_sparse_attention_pks_gb300 import pks  # noqa: E402
 from top_sparse_attention_pks_gb300.decoder import MlaDecodeStep, SparseDecodeStep  # noqa: E402
 from top_sparse_attention_pks_gb300.workloads import (MLA_LATENT, MLA_WORKLOADS,  # noqa: E402
-                                                      WORKLOADS, draw_host, draw_mla_tensors,
-                                                      draw_tensors)
+                                                      WORKLOADS, draw_float_weights, draw_host,
+                                                      draw_mla_tensors, draw_tensors)
 
 METRIC = "sparse decode steps/s"
 UNIT = "steps/s"
@@ -153,9 +153,16 @@ def oracle_request_step(wl, t_host, b, n_tokens):
     import oracle
     P = wl.page_size
     lens = np.array([n_tokens], np.int32)
-    scores = oracle.indexer_scores(lens, t_host["bt"][b: b + 1], P, t_host["q_idx"][b: b + 1],
-                                   t_host["w_idx"], t_host["idx_k"])
-    idx = oracle.topk(lens, scores, wl.k)
+    if t_host.get("w_f") is not None:  # real-valued head weights
+        scores = oracle.indexer_scores_f(lens, t_host["bt"][b: b + 1], P,
+                                         t_host["q_idx"][b: b + 1], t_host["w_f"][b: b + 1],
+                                         t_host["idx_k"])
+        idx = oracle.topk_f(lens, scores, wl.k)
+    else:
+        scores = oracle.indexer_scores(lens, t_host["bt"][b: b + 1], P,
+                                       t_host["q_idx"][b: b + 1], t_host["w_idx"],
+                                       t_host["idx_k"])
+        idx = oracle.topk(lens, scores, wl.k)
     oracle.sparse_attention(t_host["bt"][b: b + 1], P, idx, t_host["q"][b: b + 1],
                             t_host["kv_k"], t_host["kv_v"])
 
@@ -171,7 +178,8 @@ def oracle_inputs(wl, t, b):
     return dict(bt=cbt, q_idx=t["q_idx"].cpu().numpy(), w_idx=t["w_idx"].cpu().numpy(),
                 q=t["q"].cpu(), idx_k=t["idx_k"].index_select(0, pages).cpu().numpy(),
                 kv_k=t["kv_k"].index_select(0, pages).cpu(),
-                kv_v=t["kv_v"].index_select(0, pages).cpu(), len=int(lens[b]))
+                kv_v=t["kv_v"].index_select(0, pages).cpu(), len=int(lens[b]),
+                w_f=t["w_idx_f"].cpu().numpy() if "w_idx_f" in t else None)
 
 
 def time_oracle(wl, t, budget_s, min_reps=1, steps=None, warmup=0):
@@ -237,6 +245,11 @@ def main():
     ap.add_argument("--hisparse", action="store_true",
                     help="workloads with a slot table: K/V in pinned host memory, HBM slots, "
                          "misses fetched every step (select, update, fetch, attention)")
+    ap.add_argument("--float-weights", action="store_true",
+                    help="real-valued indexer head weights, float [B, Hi] (fp32 scores), "
+                         "uniform in [0.25, 2)")
+    ap.add_argument("--signed-weights", action="store_true",
+                    help="with --float-weights: weights uniform in [-2, 2)")
     ap.add_argument("--mla", action="store_true",
                     help="the DSA step with sparse MLA attention (MQA mode, tcgen05): "
                          "indexer scan, top-k, MLA over the selection; default workload "
@@ -287,6 +300,8 @@ def main():
         t["q_idx"] = torch.randint(-127, 128, (wl.B, args.queries, wl.Hi, wl.Di),
                                    dtype=torch.int8, device=dev, generator=gen)
         args.no_cpu_baseline = True
+    if args.float_weights:
+        t["w_idx_f"] = draw_float_weights(wl, dev, seed_offset=rank, signed=args.signed_weights)
 
     if args.impl == "reference":
         ref = time_oracle(wl, t, budget_s=120.0, steps=args.steps, warmup=args.warmup)
@@ -812,6 +827,9 @@ def config_dict(wl, args):
             "indexer_heads_dim": [wl.Hi, wl.Di], "indexer_dtype": "int8", "top_k": wl.k,
             "kv_dtype": "bf16", "prefix": [wl.prefix_len, wl.group_size],
             "query_tokens": getattr(args, "queries", 1),
+            "indexer_weights": ("float32 [B, Hi] U[-2,2)" if getattr(args, "signed_weights", False)
+                                else "float32 [B, Hi] U[0.25,2)")
+            if getattr(args, "float_weights", False) else "int32 [Hi] (ones)",
             "residency_slots": wl.capacity, "parallelism": f"replicas x{args.gpus}",
             "l2": "flushed between timed steps (256 MB write, outside the timed intervals)",
             "timing": "CUDA events around each CUDA-graph replay of the step"}

@@ -29,7 +29,7 @@
  * Layouts (all row-major, all device pointers unless stated "host"):
  *   q            bf16  [B, Hq, D]            attention query of the decoded token
  *   q_idx        int8  [B, Hi, Di]           indexer query (Hi heads)
- *   w_idx        int32 [Hi]                  indexer head weights
+ *   w_idx        int32 [Hi]                  indexer head weights (or w_idx_f: float [B, Hi])
  *   kv_k, kv_v   bf16  [num_pages, page_size, Hkv, D]   paged K / V pools
  *   idx_k        int8  [num_pages, page_size, Di]       paged single-head indexer keys
  *   seq_lens     int32 [B]                   cached tokens per request (0 allowed)
@@ -172,6 +172,16 @@ typedef struct pks_decode_args {
                              Nq in {1, 2, 4, 8} and Hi * Nq <= 8 (UNSUPPORTED otherwise);
                              pks_indexer_scores then writes B * Nq score rows */
   int32_t reserved[1];    /* must be 0 */
+  const float* w_idx_f;   /* NULL, or real-valued indexer head weights, device float
+                             [B, Hi] (one row per request; n_queries must then be 1):
+                             s[b,t] = sum_h w_idx_f[b,h] * max(0, q_idx[b,h,:] . k_idx(b,t))
+                             evaluated in fp32 with the heads in order, each product and
+                             each sum rounded to nearest (no fused multiply-add); w_idx is
+                             then not read.  The scores the scan writes (and
+                             pks_indexer_scores returns) are int32 keys with the order of
+                             the fp32 scores: key = bits(s) for s >= 0, bits(s) ^ 0x7fffffff
+                             for s < 0 (-0 taken as +0).  Weights must keep every score
+                             finite. */
 } pks_decode_args;
 
 /* Workspace bytes a step with these shapes needs (pointers may be NULL). */

@@ -31,6 +31,24 @@ __device__ __forceinline__ int score_bin(int s) {
   return s > 0 ? kScoreBins / 2 + 1 + v : kScoreBins / 2 - 1 - v;
 }
 
+// Real-valued head weights: the fp32 score is stored as an int32 key with the
+// same order (negative scores have their magnitude bits flipped; -0 becomes
+// +0 first, so equal scores give equal keys).
+__device__ __forceinline__ int float_key(float f) {
+  const int b = __float_as_int(__fadd_rn(f, 0.f));
+  return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ int key_bin(int key) {
+  // the fp32 score's magnitude bits; bins as for integer scores: 32 per
+  // octave of |score| from 1 up (exponent and top five mantissa bits), one
+  // bin for |score| < 1, the top bin from 2^31 up
+  const uint32_t a = (uint32_t)(key >= 0 ? key : key ^ 0x7fffffff) & 0x7fffffffu;
+  if (a < 0x3f800000u) return kScoreBins / 2;
+  const int e = (int)(a >> 23) - 127;
+  const int v = e > 30 ? 30 * 32 + 31 : e * 32 + (int)((a >> 18) & 31u);
+  return key >= 0 ? kScoreBins / 2 + 1 + v : kScoreBins / 2 - 1 - v;
+}
+
 // Score store with an L2 evict-last policy: the top-k reads the scores right
 // after the scan, while the keys stream through L2 with evict-first loads.
 __device__ __forceinline__ void store_score_keep(int32_t* p, int v) {
@@ -94,10 +112,14 @@ __device__ __forceinline__ void imma_16832(int (&c)[4], int a0, int a1, int a2, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int HI, int DI, int NT, int NQ>
+// FW: real-valued head weights w_f [B * NQ, HI] instead of the integer w_idx
+// [HI]; the score of a (token, query) is then the fp32 sum over the heads in
+// order of w * ReLU(dot), each product and sum rounded to nearest.
+template <int HI, int DI, int NT, int NQ, bool FW>
 __global__ void __launch_bounds__(NT, 1)
 k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                    const int8_t* __restrict__ q_idx, const int32_t* __restrict__ w_idx,
+                   const float* __restrict__ w_f,
                    const int8_t* __restrict__ idx_k, int32_t* __restrict__ scores, int64_t ld,
                    int32_t* __restrict__ hist, int32_t* __restrict__ err, int B, int max_pages,
                    int page_size, int page_shift, int num_pages, int k) {
@@ -110,8 +132,9 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   pdl_launch_dependents();
   int* s_hist = smem_i;                      // [NQ][kScoreBins]
   int* s_prefix = smem_i + NQ * kScoreBins;  // [B + 1]
-  // NQ > 1: weighted ReLU of each (token, query head) of a warp's round
-  __shared__ int s_ep[NQ > 1 ? NT / 32 : 1][32][8];
+  // NQ > 1 or FW: (weighted) ReLU of each (token, query head) of a warp's round
+  constexpr bool kTile = NQ > 1 || FW;
+  __shared__ int s_ep[kTile ? NT / 32 : 1][32][8];
   __shared__ int s_warp[NT / 32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -220,6 +243,7 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   // query head n of the MMA's N = 8 columns: query n / HI, indexer head n % HI
   int4 qf[HALVES];  // chunks 4*hv + tq of query head gq (zero for padding)
   int w0 = 0, w1 = 0;  // weights of query heads 2tq and 2tq+1
+  float wf[FW ? HI * NQ : 1];  // FW: the request's real weights, query-major
   int cb = -1, cb_len = 0, cb_first = 0, cb_next = 0;
   bool do_hist = false;
   // output token of this lane: tile (tq >> 1), row gq + 8 * (tq & 1)
@@ -255,11 +279,17 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
                      ? __ldg(reinterpret_cast<const int4*>(q_idx + ((int64_t)b * NQ * HI + gq) * DI) +
                              4 * hv + tq)
                      : make_int4(0, 0, 0, 0);
-      w0 = 2 * tq < HI * NQ ? __ldg(w_idx + (2 * tq) % HI) : 0;
-      w1 = 2 * tq + 1 < HI * NQ ? __ldg(w_idx + (2 * tq + 1) % HI) : 0;
+      if constexpr (FW) {
+        w0 = w1 = 1;  // the tile keeps the plain ReLU; the real weights come after
+#pragma unroll
+        for (int i = 0; i < HI * NQ; ++i) wf[i] = __ldg(w_f + (int64_t)b * NQ * HI + i);
+      } else {
+        w0 = 2 * tq < HI * NQ ? __ldg(w_idx + (2 * tq) % HI) : 0;
+        w1 = 2 * tq + 1 < HI * NQ ? __ldg(w_idx + (2 * tq + 1) % HI) : 0;
+      }
     }
 
-    if constexpr (NQ > 1) {
+    if constexpr (kTile) {
       // weighted ReLU of every (token, query head) into the warp's tile; then
       // lane L sums the HI heads of each query for token L of the round
 #pragma unroll
@@ -283,10 +313,19 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
         int score = 0;
+        if constexpr (FW) {
+          float sf = 0.f;
 #pragma unroll
-        for (int h = 0; h < HI; ++h) score += s_ep[warp][lane][q * HI + h];
+          for (int h = 0; h < HI; ++h)
+            sf = __fadd_rn(sf, __fmul_rn(wf[q * HI + h], (float)s_ep[warp][lane][q * HI + h]));
+          score = float_key(sf);
+        } else {
+#pragma unroll
+          for (int h = 0; h < HI; ++h) score += s_ep[warp][lane][q * HI + h];
+        }
         if (valid) store_score_keep(scores + ((int64_t)cb * NQ + q) * ld + t, score);
-        if (do_hist && valid) atomicAdd(&s_hist[q * kScoreBins + score_bin(score)], 1);
+        if (do_hist && valid)
+          atomicAdd(&s_hist[q * kScoreBins + (FW ? key_bin(score) : score_bin(score))], 1);
       }
       __syncwarp();  // the tile is rewritten next round
       return;
@@ -356,7 +395,7 @@ cudaError_t raise_smem(K kern, size_t smem, size_t (&configured)[64]) {
 // threads a CTA (one CTA an SM)
 constexpr int kMmaThreads = 1024;
 
-template <int HI, int DI, int NQ>
+template <int HI, int DI, int NQ, bool FW = false>
 cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld, int32_t* hist,
                           int32_t* err, cudaStream_t s) {
   int shift = -1;
@@ -366,11 +405,11 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
   }
   static size_t configured[64] = {0};  // per instantiation
   const size_t smem = sizeof(int) * ((size_t)NQ * kScoreBins + a.B + 1);
-  auto kern = k_indexer_scan_mma<HI, DI, kMmaThreads, NQ>;
+  auto kern = k_indexer_scan_mma<HI, DI, kMmaThreads, NQ, FW>;
   cudaError_t e = raise_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   kern<<<device_sm_count(), kMmaThreads, smem, s>>>(a.seq_lens, a.block_table, a.q_idx, a.w_idx,
-                                                    a.idx_k, scores, ld, hist, err, a.B,
+                                                    a.w_idx_f, a.idx_k, scores, ld, hist, err, a.B,
                                                     a.max_pages, a.page_size, shift, a.num_pages,
                                                     a.k);
   return cudaGetLastError();
@@ -381,6 +420,20 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
 cudaError_t launch_indexer_scan(const pks_decode_args& a, int32_t* scores, int64_t ld,
                                 int32_t* hist, int32_t* err, cudaStream_t s) {
   const int nq = query_count(a);
+  if (a.w_idx_f) {  // real-valued head weights: one query token per request
+#define PKS_SCAN_FW(HI_, DI_) \
+  if (a.Hi == HI_ && a.Di == DI_) return launch_scan_t<HI_, DI_, 1, true>(a, scores, ld, hist, err, s);
+    PKS_SCAN_FW(1, 64)
+    PKS_SCAN_FW(2, 64)
+    PKS_SCAN_FW(4, 64)
+    PKS_SCAN_FW(8, 64)
+    PKS_SCAN_FW(1, 128)
+    PKS_SCAN_FW(2, 128)
+    PKS_SCAN_FW(4, 128)
+    PKS_SCAN_FW(8, 128)
+#undef PKS_SCAN_FW
+    return cudaErrorInvalidValue;
+  }
 #define PKS_SCAN_CASE(HI_, DI_, NQ_)                       \
   if (a.Hi == HI_ && a.Di == DI_ && nq == NQ_)             \
     return launch_scan_t<HI_, DI_, NQ_>(a, scores, ld, hist, err, s);

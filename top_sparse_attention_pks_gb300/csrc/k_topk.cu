@@ -52,6 +52,22 @@ __device__ __forceinline__ int score_bin(int s) {
   return s > 0 ? kScoreBins / 2 + 1 + v : kScoreBins / 2 - 1 - v;
 }
 
+// Scores from real-valued head weights are order-preserving int32 keys of the
+// fp32 score (the scan bins them the same way).
+__device__ __forceinline__ int key_bin(int key) {
+  // the fp32 score's magnitude bits; bins as for integer scores: 32 per
+  // octave of |score| from 1 up (exponent and top five mantissa bits), one
+  // bin for |score| < 1, the top bin from 2^31 up
+  const uint32_t a = (uint32_t)(key >= 0 ? key : key ^ 0x7fffffff) & 0x7fffffffu;
+  if (a < 0x3f800000u) return kScoreBins / 2;
+  const int e = (int)(a >> 23) - 127;
+  const int v = e > 30 ? 30 * 32 + 31 : e * 32 + (int)((a >> 18) & 31u);
+  return key >= 0 ? kScoreBins / 2 + 1 + v : kScoreBins / 2 - 1 - v;
+}
+__device__ __forceinline__ int score_bin_m(int s, bool fkey) {
+  return fkey ? key_bin(s) : score_bin(s);
+}
+
 // Larger key = earlier in the (score descending, index ascending) order.
 __device__ __forceinline__ uint64_t order_key(int score, int t) {
   return ((uint64_t)((uint32_t)score ^ 0x80000000u) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)t);
@@ -112,6 +128,7 @@ struct TopkWs {
   int32_t* chunk_off;  // [B][nchunks]      output offset per chunk (long requests)
   TopkThreshold* thr;  // [B]
   int32_t* err;
+  int fkey;            // scores are keys of fp32 scores (real-valued head weights)
 };
 
 // Shared memory of the chunk phase and the exact select.
@@ -136,7 +153,7 @@ __device__ __forceinline__ bool chunk_phase(const int32_t* __restrict__ sb, cons
                                             int32_t* cand_n,
                                             uint32_t* bw, bool bitmap, int32_t* err, bool report,
                                             int (&sc)[kPerThread], int& T1, int& above,
-                                            int& gt_total, TopkSmem& sm) {
+                                            int& gt_total, TopkSmem& sm, bool fkey) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // chunk scores first (independent of the histogram): one L2 latency
 #pragma unroll
@@ -189,7 +206,7 @@ __device__ __forceinline__ bool chunk_phase(const int32_t* __restrict__ sb, cons
   for (int j = 0; j < kPerThread; ++j) {
     const int t = start + j * kTopkThreads + tid;
     const bool valid = t < stop;
-    const int bin = score_bin(sc[j]);
+    const int bin = score_bin_m(sc[j], fkey);
     // slice j of warp `warp` is the aligned 32-token word at t - lane
     const unsigned m = __ballot_sync(0xffffffffu, valid && bin > T1);
     if (lane == 0) {
@@ -269,7 +286,26 @@ constexpr int kSpecSlots = 2 * kTopkThreads;              // candidates read wit
 
 // Score range [lo, hi] of a non-empty histogram bin (the inverse of
 // score_bin on the scores that reach the bin).
-__device__ __forceinline__ void bin_range(int bin, int& lo, int& hi) {
+__device__ __forceinline__ void bin_range(int bin, int& lo, int& hi, bool fkey) {
+  if (fkey) {  // the keys of the fp32 scores that key_bin puts in `bin`
+    if (bin == kScoreBins / 2) {  // |score| < 1
+      lo = (int)(0xbf7fffffu ^ 0x7fffffffu);
+      hi = 0x3f7fffff;
+      return;
+    }
+    const bool pos = bin > kScoreBins / 2;
+    const int v = pos ? bin - (kScoreBins / 2 + 1) : (kScoreBins / 2 - 1) - bin;
+    const uint32_t alo = ((uint32_t)((v >> 5) + 127) << 23) | ((uint32_t)(v & 31) << 18);
+    const uint32_t ahi = v == 30 * 32 + 31 ? 0x7fffffffu : alo | 0x3ffffu;
+    if (pos) {
+      lo = (int)alo;
+      hi = (int)ahi;
+    } else {  // key = ~magnitude bits for negative scores: larger magnitude, smaller key
+      lo = (int)(0xffffffffu - ahi);
+      hi = (int)(0xffffffffu - alo);
+    }
+    return;
+  }
   if (bin == kScoreBins / 2) {
     lo = hi = 0;
     return;
@@ -451,7 +487,7 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
         sm.T1 = tid * kPer + i;
         sm.above = run;
         int lo, hi;
-        bin_range(tid * kPer + i, lo, hi);
+        bin_range(tid * kPer + i, lo, hi, w.fkey != 0);
         s_lo = lo;
         s_hi = hi;
       }
@@ -683,7 +719,8 @@ k_topk_threshold(const int32_t* __restrict__ seq_lens, const int32_t* __restrict
   int sc[kPerThread];
   int T1, above, gt_total;
   if (!chunk_phase(scores + (int64_t)b * ld, w.hist + (int64_t)b * kScoreBins, start, stop, k,
-                   cb, max_len, w.cand_n + b, bw, true, w.err, c == 0, sc, T1, above, gt_total, sm))
+                   cb, max_len, w.cand_n + b, bw, true, w.err, c == 0, sc, T1, above, gt_total, sm,
+                   w.fkey != 0))
     return;
   if (tid == 0) w.gt_cnt[(int64_t)b * nchunks_max + c] = gt_total;
 
@@ -837,6 +874,7 @@ TopkWs topk_ws(const WorkspaceLayout& L, uint8_t* ws) {
   w.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
   w.thr = reinterpret_cast<TopkThreshold*>(ws + L.thresh);
   w.err = reinterpret_cast<int32_t*>(ws + L.err);
+  w.fkey = 0;
   return w;
 }
 
@@ -870,7 +908,8 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
   const int max_len = a.max_pages * a.page_size;
   const int nq = query_count(a);
   const dim3 grid(L.nchunks, a.B * nq);  // virtual requests
-  const TopkWs w = topk_ws(L, ws);
+  TopkWs w = topk_ws(L, ws);
+  w.fkey = a.w_idx_f != nullptr ? 1 : 0;
   const int32_t* scores = reinterpret_cast<const int32_t*>(ws + L.scores);
   if (topk_single_launch(a, L)) {
     // cooperative: the launch fails rather than run with CTAs of a request

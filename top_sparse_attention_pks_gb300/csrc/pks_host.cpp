@@ -55,6 +55,7 @@ pks_status check_shapes(const pks_decode_args* a) {
   const int nq = query_count(*a);
   if ((nq & (nq - 1)) != 0 || (int64_t)a->Hi * nq > 8) return PKS_ERR_UNSUPPORTED;
   if ((int64_t)a->B * query_count(*a) > kMaxB) return PKS_ERR_UNSUPPORTED;
+  if (a->w_idx_f && nq > 1) return PKS_ERR_UNSUPPORTED;  // real weights: one query token
   if ((int64_t)a->num_pages * a->page_size > INT32_MAX) return PKS_ERR_UNSUPPORTED;
   if (a->D != 64 && a->D != 128) return PKS_ERR_UNSUPPORTED;
   if (a->Di != 64 && a->Di != 128) return PKS_ERR_UNSUPPORTED;
@@ -73,7 +74,7 @@ pks_status check_common_ptrs(const pks_decode_args* a) {
 
 pks_status check_scan_ptrs(const pks_decode_args* a) {
   if (a->B == 0) return PKS_OK;
-  if (!a->q_idx || !a->w_idx || !a->idx_k) return PKS_ERR_INVALID;
+  if (!a->q_idx || (!a->w_idx && !a->w_idx_f) || !a->idx_k) return PKS_ERR_INVALID;
   if (!aligned16(a->q_idx) || !aligned16(a->idx_k)) return PKS_ERR_INVALID;
   return PKS_OK;
 }

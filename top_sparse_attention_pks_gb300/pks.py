@@ -49,6 +49,7 @@ class pks_decode_args(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("attn_splits", ctypes.c_int32), ("topk_mode", ctypes.c_int32),
         ("n_queries", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1),
+        ("w_idx_f", ctypes.c_void_p),
     ]
 
 
@@ -277,7 +278,8 @@ class Pool:
 
 def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: int,
               topk_idx=None, out=None, workspace=None, attn_splits: int = 0,
-              topk_mode: int = 0, num_pages: Optional[int] = None) -> pks_decode_args:
+              topk_mode: int = 0, num_pages: Optional[int] = None,
+              w_idx_f=None) -> pks_decode_args:
     """Fill a ``pks_decode_args`` from tensors (shapes are read off the tensors).
 
     ``q`` is [B, Hq, D], or [B, Nq, Hq, D] for Nq query tokens per request (then
@@ -317,7 +319,15 @@ def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: i
         a.workspace_bytes = workspace.numel()
     a.attn_splits = int(attn_splits)
     a.topk_mode = int(topk_mode)
+    a.w_idx_f = _dptr(w_idx_f, torch.float32, "w_idx_f")
     return a
+
+
+def float_key_to_score(keys: np.ndarray) -> np.ndarray:
+    """The fp32 scores behind the int32 keys the scan writes with real weights."""
+    k = np.asarray(keys, dtype=np.int32)
+    bits = np.where(k >= 0, k, k ^ np.int32(0x7fffffff))
+    return bits.astype(np.int32).view(np.float32)
 
 
 def pks_decode_workspace_size(args: pks_decode_args) -> int:

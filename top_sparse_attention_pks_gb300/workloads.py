@@ -200,3 +200,12 @@ def draw_mla_tensors(wl: Workload, device="cpu", seed_offset: int = 0) -> dict:
     q, q_idx = draw_queries(wl, device, seed_offset)
     w_idx = torch.ones(wl.Hi, dtype=torch.int32, device=device)
     return dict(q=q, q_idx=q_idx, w_idx=w_idx, kv=kv, idx_k=idx_k)
+
+
+def draw_float_weights(wl: Workload, device="cpu", seed_offset: int = 0, signed: bool = False):
+    """Real-valued indexer head weights, float32 [B, Hi]: uniform in [0.25, 2)
+    (or [-2, 2) when ``signed``), one row per request."""
+    g = _gen("cpu", wl.seed * 4099 + 31 * seed_offset + 5)
+    u = torch.rand((wl.B, wl.Hi), generator=g, dtype=torch.float32)
+    w = u * 4.0 - 2.0 if signed else 0.25 + u * 1.75
+    return w.to(device)
