@@ -100,3 +100,34 @@ def test_float_weights_reject_several_query_tokens():
     import ctypes
     n = ctypes.c_size_t()
     assert pks.lib().pks_decode_workspace_size(ctypes.byref(a), ctypes.byref(n)) == -6
+
+
+@pytest.mark.parametrize("topk_mode", [0, 1])
+def test_all_tied_scores_take_the_lowest_tokens(topk_mode):
+    # zero head weights: every token scores 0, so the top-k of a request longer
+    # than k is its first k tokens
+    wl = WORKLOADS["b32_4k"]
+    t, _, _ = prepare(wl)
+    t["w_idx"] = torch.zeros((wl.Hi,), dtype=torch.int32, device="cuda")
+    step = SparseDecodeStep(t, wl.k, topk_mode=topk_mode)
+    _, idx = step()
+    torch.cuda.synchronize()
+    assert step.device_error() == 0
+    want = np.tile(np.arange(wl.k, dtype=np.int32), (wl.B, 1))
+    np.testing.assert_array_equal(host(idx).numpy(), want)
+
+
+def test_negative_weights_thousands_of_zero_ties_full_size():
+    # weights all negative: about len/16 tokens tie at the largest score, 0
+    wl = WORKLOADS["b16_128k"]
+    t, _, _ = prepare(wl)
+    t["w_idx_f"] = -draw_float_weights(wl, "cuda")
+    step = SparseDecodeStep(t, wl.k)
+    _, idx = step()
+    torch.cuda.synchronize()
+    assert step.device_error() == 0
+    req = [0, 9]
+    _, ref_idx = _oracle_f(wl, t, t["w_idx_f"], requests=req)
+    assert (host(idx).numpy()[req] == ref_idx).all(), "top-k indices differ"
+    del t, step
+    torch.cuda.empty_cache()

@@ -39,13 +39,15 @@ __device__ __forceinline__ int float_key(float f) {
   return b >= 0 ? b : b ^ 0x7fffffff;
 }
 __device__ __forceinline__ int key_bin(int key) {
-  // the fp32 score's magnitude bits; bins as for integer scores: 32 per
-  // octave of |score| from 1 up (exponent and top five mantissa bits), one
-  // bin for |score| < 1, the top bin from 2^31 up
+  // the fp32 score's magnitude bits a: exact zero alone in the middle bin;
+  // |score| < 1 one bin per octave down to 2^-32; from 1 up 32 bins per
+  // octave (exponent and top five mantissa bits), the top bin from 2^30 up
   const uint32_t a = (uint32_t)(key >= 0 ? key : key ^ 0x7fffffff) & 0x7fffffffu;
-  if (a < 0x3f800000u) return kScoreBins / 2;
+  if (a == 0) return kScoreBins / 2;
   const int e = (int)(a >> 23) - 127;
-  const int v = e > 30 ? 30 * 32 + 31 : e * 32 + (int)((a >> 18) & 31u);
+  int v;
+  if (e < 0) v = e < -32 ? 0 : 32 + e;
+  else v = 32 + (e > 29 ? 29 * 32 + 31 : e * 32 + (int)((a >> 18) & 31u));
   return key >= 0 ? kScoreBins / 2 + 1 + v : kScoreBins / 2 - 1 - v;
 }
 

@@ -55,13 +55,15 @@ __device__ __forceinline__ int score_bin(int s) {
 // Scores from real-valued head weights are order-preserving int32 keys of the
 // fp32 score (the scan bins them the same way).
 __device__ __forceinline__ int key_bin(int key) {
-  // the fp32 score's magnitude bits; bins as for integer scores: 32 per
-  // octave of |score| from 1 up (exponent and top five mantissa bits), one
-  // bin for |score| < 1, the top bin from 2^31 up
+  // the fp32 score's magnitude bits a: exact zero alone in the middle bin;
+  // |score| < 1 one bin per octave down to 2^-32; from 1 up 32 bins per
+  // octave (exponent and top five mantissa bits), the top bin from 2^30 up
   const uint32_t a = (uint32_t)(key >= 0 ? key : key ^ 0x7fffffff) & 0x7fffffffu;
-  if (a < 0x3f800000u) return kScoreBins / 2;
+  if (a == 0) return kScoreBins / 2;
   const int e = (int)(a >> 23) - 127;
-  const int v = e > 30 ? 30 * 32 + 31 : e * 32 + (int)((a >> 18) & 31u);
+  int v;
+  if (e < 0) v = e < -32 ? 0 : 32 + e;
+  else v = 32 + (e > 29 ? 29 * 32 + 31 : e * 32 + (int)((a >> 18) & 31u));
   return key >= 0 ? kScoreBins / 2 + 1 + v : kScoreBins / 2 - 1 - v;
 }
 __device__ __forceinline__ int score_bin_m(int s, bool fkey) {
@@ -139,6 +141,7 @@ struct TopkSmemT {
   int T1, above, flag;
   int digit, digit_above, digit_count;
   int cand_base;
+  int tied;  // select_threshold took the one-score shortcut
   unsigned long long kand[NT / 32], kor[NT / 32];
 };
 using TopkSmem = TopkSmemT<kTopkThreads>;
@@ -288,15 +291,21 @@ constexpr int kSpecSlots = 2 * kTopkThreads;              // candidates read wit
 // score_bin on the scores that reach the bin).
 __device__ __forceinline__ void bin_range(int bin, int& lo, int& hi, bool fkey) {
   if (fkey) {  // the keys of the fp32 scores that key_bin puts in `bin`
-    if (bin == kScoreBins / 2) {  // |score| < 1
-      lo = (int)(0xbf7fffffu ^ 0x7fffffffu);
-      hi = 0x3f7fffff;
+    if (bin == kScoreBins / 2) {  // exact zero (-0 is stored as +0)
+      lo = hi = 0;
       return;
     }
     const bool pos = bin > kScoreBins / 2;
     const int v = pos ? bin - (kScoreBins / 2 + 1) : (kScoreBins / 2 - 1) - bin;
-    const uint32_t alo = ((uint32_t)((v >> 5) + 127) << 23) | ((uint32_t)(v & 31) << 18);
-    const uint32_t ahi = v == 30 * 32 + 31 ? 0x7fffffffu : alo | 0x3ffffu;
+    uint32_t alo, ahi;
+    if (v < 32) {  // one octave of |score| < 1 (v = 0: everything below 2^-31)
+      alo = v == 0 ? 1u : (uint32_t)(v - 32 + 127) << 23;
+      ahi = ((uint32_t)(v - 32 + 128) << 23) - 1u;
+    } else {
+      const int u = v - 32;
+      alo = ((uint32_t)((u >> 5) + 127) << 23) | ((uint32_t)(u & 31) << 18);
+      ahi = u == 29 * 32 + 31 ? 0x7fffffffu : alo | 0x3ffffu;
+    }
     if (pos) {
       lo = (int)alo;
       hi = (int)ahi;
@@ -333,10 +342,12 @@ __device__ __forceinline__ void bin_range(int bin, int& lo, int& hi, bool fkey) 
 // Exact threshold key among the n candidates: the need-th largest
 // (score, ~token) key, radix-selected 8 bits at a time after the leading bits
 // that every candidate shares.  Block-wide (NT threads); every thread returns
-// the key.
+// the key.  `ordered`: key_at(0..n-1) lists the candidates in ascending token
+// order, so when they all share one score the need-th largest key is simply
+// the need-th candidate (many exact ties, e.g. at score 0).
 template <int NT, typename KeyAt>
 __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_at,
-                                                     TopkSmemT<NT>& sm) {
+                                                     TopkSmemT<NT>& sm, bool ordered = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint64_t kand = ~0ull, kor = 0ull;
   for (int i = tid; i < n; i += NT) {
@@ -362,6 +373,9 @@ __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_
     kor |= sm.kor[i];
   }
   const int common = n > 0 ? __clzll((long long)(kand ^ kor)) : 64;  // 64 when all equal
+  const bool tied = ordered && common >= 32 && need >= 1 && need <= n;
+  if (tid == 0) sm.tied = tied ? 1 : 0;  // read by the caller after its next barrier
+  if (tied) return key_at(need - 1);
   int bits = (common / 8) * 8;
   uint64_t prefix = bits == 0 ? 0ull : (bits == 64 ? kand : (kand >> (64 - bits)));
   while (bits < 64) {
@@ -635,12 +649,19 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
     const int2 e = cand_at(i);
     return order_key(e.x, e.y);
   };
-  const uint64_t kstar = select_threshold(n, k - above, key_at, sm);
+  // candidates are in token order (chunk regions in chunk order)
+  const int need = k - above;
+  const uint64_t kstar = select_threshold(n, need, key_at, sm, /*ordered=*/true);
+  __syncthreads();
+  // one score among all candidates: the selected ones are the first `need`
+  // in token order, so positions decide without reading the keys again
+  const bool tied = sm.tied != 0;
 
   // ---- output offset: above-T1 tokens and selected candidates of earlier chunks
   int before = 0;
-  for (int i = tid; i < s_eqoff[c]; i += kTopkThreads) before += key_at(i) >= kstar;
-  before = s_before + block_sum<kTopkThreads>(before, sm.warp);
+  if (!tied)
+    for (int i = tid; i < s_eqoff[c]; i += kTopkThreads) before += key_at(i) >= kstar;
+  before = s_before + (tied ? min(s_eqoff[c], need) : block_sum<kTopkThreads>(before, sm.warp));
 
   // ---- this chunk's selected tokens, ascending: this thread's candidates sit
   // in the request's list in token order from its chunk's offset plus its
@@ -651,7 +672,7 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
 #pragma unroll
     for (int bit = 0; bit < kTokPerThread; ++bit)
       if ((eqm >> bit) & 1u) {
-        if (key_at(i) >= kstar) selm |= 1u << bit;
+        if (tied ? i < need : key_at(i) >= kstar) selm |= 1u << bit;
         ++i;
       }
   }
