@@ -86,6 +86,11 @@ def _declare(L):
     L.orc_indexer_scores_f.argtypes = [_I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P,
                                        _I64]
     L.orc_indexer_scores_f.restype = ctypes.c_int
+    L.orc_e4m3_value.argtypes = [ctypes.c_uint8]
+    L.orc_e4m3_value.restype = ctypes.c_double
+    L.orc_indexer_scores_fp8.argtypes = [_I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P,
+                                         _I64]
+    L.orc_indexer_scores_fp8.restype = ctypes.c_int
     L.orc_topk_f.argtypes = [_I32, _P, _P, _I64, _I32, _P]
     L.orc_topk_f.restype = ctypes.c_int
     L.orc_mla_sparse_attention.argtypes = [_I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
@@ -205,6 +210,39 @@ def indexer_scores_f(seq_lens, block_table, page_size, q_idx, w_f, idx_k, ld=Non
     _check(lib().orc_indexer_scores_f(B, _ptr(lens), _ptr(bt), bt.shape[1], int(page_size), Hi,
                                       Di, _ptr(qi), _ptr(wf), _ptr(ik), _ptr(out), int(ld)),
            "indexer_scores_f")
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    return lib().orc_e4m3_value(int(code) & 0xFF)
+
+
+def _bytes(x):
+    """uint8 view of int8 / uint8 / float8 tensors or arrays."""
+    if hasattr(x, "detach"):
+        import torch
+        t = x.detach().cpu().contiguous()
+        if t.dtype != torch.uint8:
+            t = t.view(torch.uint8)
+        return t.numpy()
+    a = np.ascontiguousarray(np.asarray(x))
+    return a.view(np.uint8) if a.dtype != np.uint8 else a
+
+
+def indexer_scores_fp8(seq_lens, block_table, page_size, q_idx, w_f, idx_k, ld=None):
+    """Exact FP8 e4m3 indexer scores (float64 [B, ld])."""
+    lens = _arr(seq_lens, np.int32)
+    bt = _arr(block_table, np.int32)
+    qi = _bytes(q_idx)
+    ik = _bytes(idx_k)
+    wf = _arr(w_f, np.float32)
+    B, Hi, Di = qi.shape
+    if ld is None:
+        ld = int(bt.shape[1]) * int(page_size)
+    out = np.zeros((B, ld), dtype=np.float64)
+    _check(lib().orc_indexer_scores_fp8(B, _ptr(lens), _ptr(bt), bt.shape[1], int(page_size), Hi,
+                                        Di, _ptr(qi), _ptr(wf), _ptr(ik), _ptr(out), int(ld)),
+           "indexer_scores_fp8")
     return out
 
 

@@ -230,6 +230,55 @@ int orc_indexer_scores_f(int32_t B, const int32_t* lens, const int32_t* block_ta
   return 0;
 }
 
+/* FP8 e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities, 0x7f / 0xff are NaN) as an integer multiple of 2^-9:
+ * subnormals m * 2^-9, normals (8 + m) * 2^(e - 1) * 2^-9.  Returns 0 and sets
+ * *nan for a NaN code. */
+static int64_t e4m3_units(uint8_t b, int* nan) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) {
+    *nan = 1;
+    return 0;
+  }
+  const int64_t mag = e == 0 ? (int64_t)m : (int64_t)(8 + m) << (e - 1);
+  return (b & 0x80) ? -mag : mag;
+}
+
+double orc_e4m3_value(uint8_t b) {
+  int nan = 0;
+  const int64_t u = e4m3_units(b, &nan);
+  return nan ? NAN : ldexp((double)u, -9);
+}
+
+int orc_indexer_scores_fp8(int32_t B, const int32_t* lens, const int32_t* block_table,
+                           int32_t max_pages, int32_t page_size, int32_t Hi, int32_t Di,
+                           const uint8_t* q_idx, const float* w_f, const uint8_t* idx_k,
+                           double* scores, int64_t ld) {
+  if (B < 0 || Hi <= 0 || Di <= 0 || page_size <= 0) return -3;
+  int rc = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t t = 0; t < lens[b]; ++t) {
+      const uint8_t* key = idx_k + phys_token(block_table, max_pages, page_size, b, t) * Di;
+      double s = 0.0;
+      for (int32_t h = 0; h < Hi; ++h) {
+        const uint8_t* qh = q_idx + ((int64_t)b * Hi + h) * Di;
+        /* the dot product exactly: products of 2^-9 units are 2^-18 units,
+         * the int64 sum is exact, and so is its conversion (below 2^53) */
+        int64_t dot = 0;
+        int nan = 0;
+        for (int32_t d = 0; d < Di; ++d) dot += e4m3_units(qh[d], &nan) * e4m3_units(key[d], &nan);
+        if (nan) rc = -5;
+        const double relu = dot > 0 ? ldexp((double)dot, -18) : 0.0;
+        /* [SA] weighted sum of the heads' ReLU logits (float64) */
+        s += (double)w_f[(int64_t)b * Hi + h] * relu;
+      }
+      scores[(int64_t)b * ld + t] = s;
+    }
+  }
+  return rc;
+}
+
 typedef struct {
   float score;
   int32_t t;

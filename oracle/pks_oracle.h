@@ -94,6 +94,21 @@ int orc_indexer_scores_f(int32_t B, const int32_t* lens, const int32_t* block_ta
                          const int8_t* q_idx, const float* w_f, const int8_t* idx_k,
                          float* scores, int64_t ld);
 
+/* The value of an FP8 e4m3 code (NaN for 0x7f / 0xff). */
+double orc_e4m3_value(uint8_t b);
+
+/* [SA] lightning indexer on FP8 e4m3 queries and keys with real head weights
+ *  (float [B, Hi]): s[b,t] = sum_h w_f[b,h] * max(0, q . k) with every dot
+ *  product exact (e4m3 values are integer multiples of 2^-9, so a dot is an
+ *  exact int64 count of 2^-18) and the weighted sum in float64.  This is the
+ *  exact reference the kernel's fp32 tensor-core result is held against
+ *  within a rounding bound; the selection is checked for validity against it.
+ *  Returns -5 if a NaN code occurs. */
+int orc_indexer_scores_fp8(int32_t B, const int32_t* lens, const int32_t* block_table,
+                           int32_t max_pages, int32_t page_size, int32_t Hi, int32_t Di,
+                           const uint8_t* q_idx, const float* w_f, const uint8_t* idx_k,
+                           double* scores, int64_t ld);
+
 /* orc_topk on float scores: (score descending, token ascending), -0 == +0. */
 int orc_topk_f(int32_t B, const int32_t* lens, const float* scores, int64_t ld, int32_t k,
                int32_t* idx);

@@ -209,3 +209,14 @@ def draw_float_weights(wl: Workload, device="cpu", seed_offset: int = 0, signed:
     u = torch.rand((wl.B, wl.Hi), generator=g, dtype=torch.float32)
     w = u * 4.0 - 2.0 if signed else 0.25 + u * 1.75
     return w.to(device)
+
+
+def draw_fp8_indexer(wl: Workload, device="cpu", seed_offset: int = 0):
+    """FP8 e4m3 indexer queries [B, Hi, Di] and keys [num_pages, page_size, Di]:
+    N(0, 4^2) rounded to e4m3 (finite codes only), returned as int8 tensors
+    holding the bit patterns."""
+    g = _gen(device, wl.seed * 6007 + 13 * seed_offset + 11)
+    q = (torch.randn((wl.B, wl.Hi, wl.Di), generator=g, device=device) * 4.0)
+    k = (torch.randn((wl.num_pages, wl.page_size, wl.Di), generator=g, device=device) * 4.0)
+    f8 = torch.float8_e4m3fn
+    return q.clamp(-448, 448).to(f8).view(torch.int8), k.clamp(-448, 448).to(f8).view(torch.int8)
