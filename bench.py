@@ -35,7 +35,8 @@ from top_sparse_attention_pks_gb300 import build as pkg_build  # noqa: E402
 from top_sparse_attention_pks_gb300 import pks  # noqa: E402
 from top_sparse_attention_pks_gb300.decoder import MlaDecodeStep, SparseDecodeStep  # noqa: E402
 from top_sparse_attention_pks_gb300.workloads import (MLA_LATENT, MLA_WORKLOADS,  # noqa: E402
-                                                      WORKLOADS, draw_float_weights, draw_host,
+                                                      WORKLOADS, draw_float_weights,
+                                                      draw_fp8_indexer, draw_host,
                                                       draw_mla_tensors, draw_tensors)
 
 METRIC = "sparse decode steps/s"
@@ -153,7 +154,12 @@ def oracle_request_step(wl, t_host, b, n_tokens):
     import oracle
     P = wl.page_size
     lens = np.array([n_tokens], np.int32)
-    if t_host.get("w_f") is not None:  # real-valued head weights
+    if t_host.get("fp8"):  # FP8 e4m3 indexer: exact scores, selection on their fp32 values
+        scores = oracle.indexer_scores_fp8(lens, t_host["bt"][b: b + 1], P,
+                                           t_host["q_idx"][b: b + 1], t_host["w_f"][b: b + 1],
+                                           t_host["idx_k"])
+        idx = oracle.topk_f(lens, scores.astype(np.float32), wl.k)
+    elif t_host.get("w_f") is not None:  # real-valued head weights
         scores = oracle.indexer_scores_f(lens, t_host["bt"][b: b + 1], P,
                                          t_host["q_idx"][b: b + 1], t_host["w_f"][b: b + 1],
                                          t_host["idx_k"])
@@ -179,7 +185,8 @@ def oracle_inputs(wl, t, b):
                 q=t["q"].cpu(), idx_k=t["idx_k"].index_select(0, pages).cpu().numpy(),
                 kv_k=t["kv_k"].index_select(0, pages).cpu(),
                 kv_v=t["kv_v"].index_select(0, pages).cpu(), len=int(lens[b]),
-                w_f=t["w_idx_f"].cpu().numpy() if "w_idx_f" in t else None)
+                w_f=t["w_idx_f"].cpu().numpy() if "w_idx_f" in t else None,
+                fp8=bool(t.get("idx_fp8", False)))
 
 
 def time_oracle(wl, t, budget_s, min_reps=1, steps=None, warmup=0):
@@ -250,6 +257,8 @@ def main():
                          "uniform in [0.25, 2)")
     ap.add_argument("--signed-weights", action="store_true",
                     help="with --float-weights: weights uniform in [-2, 2)")
+    ap.add_argument("--fp8-indexer", action="store_true",
+                    help="FP8 e4m3 indexer queries and keys (implies --float-weights)")
     ap.add_argument("--mla", action="store_true",
                     help="the DSA step with sparse MLA attention (MQA mode, tcgen05): "
                          "indexer scan, top-k, MLA over the selection; default workload "
@@ -300,6 +309,10 @@ def main():
         t["q_idx"] = torch.randint(-127, 128, (wl.B, args.queries, wl.Hi, wl.Di),
                                    dtype=torch.int8, device=dev, generator=gen)
         args.no_cpu_baseline = True
+    if args.fp8_indexer:
+        args.float_weights = True
+        t["q_idx"], t["idx_k"] = draw_fp8_indexer(wl, dev, seed_offset=rank)
+        t["idx_fp8"] = True
     if args.float_weights:
         t["w_idx_f"] = draw_float_weights(wl, dev, seed_offset=rank, signed=args.signed_weights)
 
@@ -824,7 +837,9 @@ def config_dict(wl, args):
             "seq_len": list(wl.seq_lens) if wl.seq_lens and len(set(wl.seq_lens)) > 1
             else (wl.seq_lens[0] if wl.seq_lens else f"U[{wl.len_lo},{wl.len_hi}]"),
             "page_size": wl.page_size, "heads_q_kv": [wl.Hq, wl.Hkv], "head_dim": wl.D,
-            "indexer_heads_dim": [wl.Hi, wl.Di], "indexer_dtype": "int8", "top_k": wl.k,
+            "indexer_heads_dim": [wl.Hi, wl.Di],
+            "indexer_dtype": "fp8 e4m3" if getattr(args, "fp8_indexer", False) else "int8",
+            "top_k": wl.k,
             "kv_dtype": "bf16", "prefix": [wl.prefix_len, wl.group_size],
             "query_tokens": getattr(args, "queries", 1),
             "indexer_weights": ("float32 [B, Hi] U[-2,2)" if getattr(args, "signed_weights", False)

@@ -182,6 +182,12 @@ typedef struct pks_decode_args {
                              the fp32 scores: key = bits(s) for s >= 0, bits(s) ^ 0x7fffffff
                              for s < 0 (-0 taken as +0).  Weights must keep every score
                              finite. */
+  int32_t idx_fp8;        /* 0: q_idx and idx_k are int8.  1: they hold FP8 e4m3 bit
+                             patterns (finite values; w_idx_f required, else INVALID); each
+                             head's dot product is taken on the tensor core with fp32
+                             accumulation in the hardware's order, then weighted and summed
+                             over the heads as for w_idx_f */
+  int32_t reserved2;      /* must be 0 */
 } pks_decode_args;
 
 /* Workspace bytes a step with these shapes needs (pointers may be NULL). */

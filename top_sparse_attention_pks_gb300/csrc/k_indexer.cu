@@ -114,10 +114,23 @@ __device__ __forceinline__ void imma_16832(int (&c)[4], int a0, int a1, int a2, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// FP8 (e4m3) queries and keys: D = A.B + C with fp32 accumulation
+__device__ __forceinline__ void fmma_e4m3_16832(float (&c)[4], int a0, int a1, int a2, int a3,
+                                                int b0, int b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // FW: real-valued head weights w_f [B * NQ, HI] instead of the integer w_idx
 // [HI]; the score of a (token, query) is then the fp32 sum over the heads in
 // order of w * ReLU(dot), each product and sum rounded to nearest.
-template <int HI, int DI, int NT, int NQ, bool FW>
+// F8 (with FW): q_idx and idx_k hold FP8 e4m3 values; each head's dot product
+// comes from the tensor core in fp32 (its accumulation order is the
+// hardware's), the weighted sum over heads as for FW.
+template <int HI, int DI, int NT, int NQ, bool FW, bool F8 = false>
 __global__ void __launch_bounds__(NT, 1)
 k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                    const int8_t* __restrict__ q_idx, const int32_t* __restrict__ w_idx,
@@ -296,18 +309,34 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
       // lane L sums the HI heads of each query for token L of the round
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        int c[4] = {0, 0, 0, 0};
+        if constexpr (F8) {
+          // fp32 ReLU of each head's dot product, kept as bits in the tile
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int hv = 0; hv < HALVES; ++hv) {
-          const int4 r0 = buf[(u * HALVES + hv) * 2 + 0];
-          const int4 r1 = buf[(u * HALVES + hv) * 2 + 1];
-          imma_16832<DI>(c, r0.x, r1.x, r0.y, r1.y, qf[hv].x, qf[hv].y);
-          imma_16832<DI>(c, r0.z, r1.z, r0.w, r1.w, qf[hv].z, qf[hv].w);
+          for (int hv = 0; hv < HALVES; ++hv) {
+            const int4 r0 = buf[(u * HALVES + hv) * 2 + 0];
+            const int4 r1 = buf[(u * HALVES + hv) * 2 + 1];
+            fmma_e4m3_16832(c, r0.x, r1.x, r0.y, r1.y, qf[hv].x, qf[hv].y);
+            fmma_e4m3_16832(c, r0.z, r1.z, r0.w, r1.w, qf[hv].z, qf[hv].w);
+          }
+          s_ep[warp][u * 16 + gq][2 * tq] = __float_as_int(fmaxf(c[0], 0.f));
+          s_ep[warp][u * 16 + gq][2 * tq + 1] = __float_as_int(fmaxf(c[1], 0.f));
+          s_ep[warp][u * 16 + gq + 8][2 * tq] = __float_as_int(fmaxf(c[2], 0.f));
+          s_ep[warp][u * 16 + gq + 8][2 * tq + 1] = __float_as_int(fmaxf(c[3], 0.f));
+        } else {
+          int c[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int hv = 0; hv < HALVES; ++hv) {
+            const int4 r0 = buf[(u * HALVES + hv) * 2 + 0];
+            const int4 r1 = buf[(u * HALVES + hv) * 2 + 1];
+            imma_16832<DI>(c, r0.x, r1.x, r0.y, r1.y, qf[hv].x, qf[hv].y);
+            imma_16832<DI>(c, r0.z, r1.z, r0.w, r1.w, qf[hv].z, qf[hv].w);
+          }
+          s_ep[warp][u * 16 + gq][2 * tq] = w0 * max(c[0], 0);
+          s_ep[warp][u * 16 + gq][2 * tq + 1] = w1 * max(c[1], 0);
+          s_ep[warp][u * 16 + gq + 8][2 * tq] = w0 * max(c[2], 0);
+          s_ep[warp][u * 16 + gq + 8][2 * tq + 1] = w1 * max(c[3], 0);
         }
-        s_ep[warp][u * 16 + gq][2 * tq] = w0 * max(c[0], 0);
-        s_ep[warp][u * 16 + gq][2 * tq + 1] = w1 * max(c[1], 0);
-        s_ep[warp][u * 16 + gq + 8][2 * tq] = w0 * max(c[2], 0);
-        s_ep[warp][u * 16 + gq + 8][2 * tq + 1] = w1 * max(c[3], 0);
       }
       __syncwarp();
       const int t = (item - cb_first) * NT + warp * 32 + lane;
@@ -318,8 +347,10 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
         if constexpr (FW) {
           float sf = 0.f;
 #pragma unroll
-          for (int h = 0; h < HI; ++h)
-            sf = __fadd_rn(sf, __fmul_rn(wf[q * HI + h], (float)s_ep[warp][lane][q * HI + h]));
+          for (int h = 0; h < HI; ++h) {
+            const int r = s_ep[warp][lane][q * HI + h];
+            sf = __fadd_rn(sf, __fmul_rn(wf[q * HI + h], F8 ? __int_as_float(r) : (float)r));
+          }
           score = float_key(sf);
         } else {
 #pragma unroll
@@ -397,7 +428,7 @@ cudaError_t raise_smem(K kern, size_t smem, size_t (&configured)[64]) {
 // threads a CTA (one CTA an SM)
 constexpr int kMmaThreads = 1024;
 
-template <int HI, int DI, int NQ, bool FW = false>
+template <int HI, int DI, int NQ, bool FW = false, bool F8 = false>
 cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld, int32_t* hist,
                           int32_t* err, cudaStream_t s) {
   int shift = -1;
@@ -407,7 +438,7 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
   }
   static size_t configured[64] = {0};  // per instantiation
   const size_t smem = sizeof(int) * ((size_t)NQ * kScoreBins + a.B + 1);
-  auto kern = k_indexer_scan_mma<HI, DI, kMmaThreads, NQ, FW>;
+  auto kern = k_indexer_scan_mma<HI, DI, kMmaThreads, NQ, FW, F8>;
   cudaError_t e = raise_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   kern<<<device_sm_count(), kMmaThreads, smem, s>>>(a.seq_lens, a.block_table, a.q_idx, a.w_idx,
@@ -422,6 +453,21 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
 cudaError_t launch_indexer_scan(const pks_decode_args& a, int32_t* scores, int64_t ld,
                                 int32_t* hist, int32_t* err, cudaStream_t s) {
   const int nq = query_count(a);
+  if (a.w_idx_f && a.idx_fp8) {  // FP8 e4m3 queries and keys, real weights
+#define PKS_SCAN_F8(HI_, DI_) \
+  if (a.Hi == HI_ && a.Di == DI_)  \
+    return launch_scan_t<HI_, DI_, 1, true, true>(a, scores, ld, hist, err, s);
+    PKS_SCAN_F8(1, 64)
+    PKS_SCAN_F8(2, 64)
+    PKS_SCAN_F8(4, 64)
+    PKS_SCAN_F8(8, 64)
+    PKS_SCAN_F8(1, 128)
+    PKS_SCAN_F8(2, 128)
+    PKS_SCAN_F8(4, 128)
+    PKS_SCAN_F8(8, 128)
+#undef PKS_SCAN_F8
+    return cudaErrorInvalidValue;
+  }
   if (a.w_idx_f) {  // real-valued head weights: one query token per request
 #define PKS_SCAN_FW(HI_, DI_) \
   if (a.Hi == HI_ && a.Di == DI_) return launch_scan_t<HI_, DI_, 1, true>(a, scores, ld, hist, err, s);

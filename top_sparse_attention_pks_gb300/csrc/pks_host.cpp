@@ -56,6 +56,8 @@ pks_status check_shapes(const pks_decode_args* a) {
   if ((nq & (nq - 1)) != 0 || (int64_t)a->Hi * nq > 8) return PKS_ERR_UNSUPPORTED;
   if ((int64_t)a->B * query_count(*a) > kMaxB) return PKS_ERR_UNSUPPORTED;
   if (a->w_idx_f && nq > 1) return PKS_ERR_UNSUPPORTED;  // real weights: one query token
+  if (a->idx_fp8 < 0 || a->idx_fp8 > 1 || a->reserved2 != 0) return PKS_ERR_INVALID;
+  if (a->idx_fp8 && !a->w_idx_f) return PKS_ERR_INVALID;  // FP8 scores need real weights
   if ((int64_t)a->num_pages * a->page_size > INT32_MAX) return PKS_ERR_UNSUPPORTED;
   if (a->D != 64 && a->D != 128) return PKS_ERR_UNSUPPORTED;
   if (a->Di != 64 && a->Di != 128) return PKS_ERR_UNSUPPORTED;

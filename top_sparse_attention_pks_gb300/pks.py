@@ -49,7 +49,7 @@ class pks_decode_args(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("attn_splits", ctypes.c_int32), ("topk_mode", ctypes.c_int32),
         ("n_queries", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1),
-        ("w_idx_f", ctypes.c_void_p),
+        ("w_idx_f", ctypes.c_void_p), ("idx_fp8", ctypes.c_int32), ("reserved2", ctypes.c_int32),
     ]
 
 
@@ -279,7 +279,7 @@ class Pool:
 def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: int,
               topk_idx=None, out=None, workspace=None, attn_splits: int = 0,
               topk_mode: int = 0, num_pages: Optional[int] = None,
-              w_idx_f=None) -> pks_decode_args:
+              w_idx_f=None, idx_fp8: bool = False) -> pks_decode_args:
     """Fill a ``pks_decode_args`` from tensors (shapes are read off the tensors).
 
     ``q`` is [B, Hq, D], or [B, Nq, Hq, D] for Nq query tokens per request (then
@@ -307,6 +307,10 @@ def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: i
     a.seq_lens = _dptr(seq_lens, torch.int32, "seq_lens")
     a.block_table = _dptr(block_table, torch.int32, "block_table")
     a.q = _dptr(q, torch.bfloat16, "q")
+    if q_idx.dtype != torch.int8:  # FP8 e4m3 tensors: their bit patterns
+        q_idx = q_idx.view(torch.int8)
+    if idx_k.dtype != torch.int8:
+        idx_k = idx_k.view(torch.int8)
     a.q_idx = _dptr(q_idx, torch.int8, "q_idx")
     a.w_idx = _dptr(w_idx, torch.int32, "w_idx")
     a.kv_k = _dptr(kv_k, torch.bfloat16, "kv_k")
@@ -320,6 +324,7 @@ def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: i
     a.attn_splits = int(attn_splits)
     a.topk_mode = int(topk_mode)
     a.w_idx_f = _dptr(w_idx_f, torch.float32, "w_idx_f")
+    a.idx_fp8 = 1 if idx_fp8 else 0
     return a
 
 
