@@ -544,10 +544,20 @@ def time_mla_oracle(wl, t, budget_s, steps=None, warmup=0):
     idx_k = t["idx_k"].index_select(0, pages).cpu().numpy()
     kv = t["kv"].index_select(0, pages).cpu()
 
+    fp8 = bool(t.get("idx_fp8", False))
+    w_f = t["w_idx_f"].cpu().numpy()[b: b + 1] if "w_idx_f" in t else None
+
     def one(n_tok):
         ln = np.array([n_tok], np.int32)
-        sc = oracle.indexer_scores(ln, cbt, wl.page_size, q_idx, w_idx, idx_k)
-        idx = oracle.topk(ln, sc, wl.k)
+        if fp8:
+            sc = oracle.indexer_scores_fp8(ln, cbt, wl.page_size, q_idx, w_f, idx_k)
+            idx = oracle.topk_f(ln, sc.astype(np.float32), wl.k)
+        elif w_f is not None:
+            sc = oracle.indexer_scores_f(ln, cbt, wl.page_size, q_idx, w_f, idx_k)
+            idx = oracle.topk_f(ln, sc, wl.k)
+        else:
+            sc = oracle.indexer_scores(ln, cbt, wl.page_size, q_idx, w_idx, idx_k)
+            idx = oracle.topk(ln, sc, wl.k)
         oracle.mla_sparse_attention(cbt, wl.page_size, idx, q, kv, MLA_LATENT)
 
     n0 = min(full, max(4 * wl.k, 8192))
@@ -579,6 +589,12 @@ def mla_bench(wl, args, dev, rank, world, dist):
     if args.topk:
         wl = wl.replace(k=args.topk)
     t, h, bt = mla_setup(wl, dev, seed_offset=rank)
+    if args.fp8_indexer:  # DSA's indexer: FP8 e4m3 queries and keys, real head weights
+        args.float_weights = True
+        t["q_idx"], t["idx_k"] = draw_fp8_indexer(wl, dev, seed_offset=rank)
+        t["idx_fp8"] = True
+    if args.float_weights:
+        t["w_idx_f"] = draw_float_weights(wl, dev, seed_offset=rank, signed=args.signed_weights)
     cfg = config_dict(wl, args)
     cfg.update({"attention": "sparse MLA, MQA mode (tcgen05)", "mla_heads": wl.Hq,
                 "latent_rope": [MLA_LATENT, wl.D - MLA_LATENT], "heads_q_kv": None,

@@ -191,3 +191,30 @@ def test_mla_full_size(name):
     check_attention(out[torch.as_tensor(req, device=out.device)], ref, name)
     del t, step
     torch.cuda.empty_cache()
+
+
+def test_dsa_step_fp8_indexer_real_weights_mla():
+    """The full DSA step: FP8 e4m3 indexer with real head weights, top-k, sparse
+    MLA.  Top-k exact against the oracle run on the GPU's own scores' order is
+    covered by the FP8 tests; here the MLA over the step's selection."""
+    from top_sparse_attention_pks_gb300.workloads import draw_float_weights, draw_fp8_indexer
+    wl = MLA_WORKLOADS["mla_paging_example"]
+    t = _prepare(wl)
+    t["q_idx"], t["idx_k"] = draw_fp8_indexer(wl, "cuda")
+    t["w_idx_f"] = draw_float_weights(wl, "cuda", signed=True)
+    t["idx_fp8"] = True
+    step = MlaDecodeStep(t, wl.k)
+    out, idx = step()
+    torch.cuda.synchronize()
+    got = host(idx).numpy()
+    lens = host(t["seq_lens"]).numpy()
+    exact = oracle.indexer_scores_fp8(lens, host(t["block_table"]).numpy(), wl.page_size,
+                                      host(t["q_idx"]), host(t["w_idx_f"]).numpy(),
+                                      host(t["idx_k"]))
+    for b, n in enumerate(lens):
+        sel = got[b][got[b] >= 0]
+        assert len(sel) == min(n, wl.k) and (np.diff(sel) > 0).all()
+        if n > wl.k:  # the exact top scores are selected up to fp32 rounding
+            unsel = np.setdiff1d(np.arange(n), sel)
+            assert exact[b, sel].min() >= exact[b, unsel].max() - 1e-3 * np.abs(exact[b, :n]).max()
+    check_attention(out, _oracle_mla(t, got, wl.page_size), "dsa step")

@@ -157,10 +157,14 @@ class MlaDecodeStep:
         a.seq_lens = pks._dptr(t["seq_lens"], torch.int32, "seq_lens")
         a.block_table = pks._dptr(t["block_table"], torch.int32, "block_table")
         a.q_idx = pks._dptr(t["q_idx"], torch.int8, "q_idx")
-        a.w_idx = pks._dptr(t["w_idx"], torch.int32, "w_idx")
+        a.w_idx = pks._dptr(t.get("w_idx"), torch.int32, "w_idx")
         a.idx_k = pks._dptr(t["idx_k"], torch.int8, "idx_k")
         a.topk_idx = pks._dptr(self.topk_idx, torch.int32, "topk_idx")
         a.topk_mode = int(topk_mode)
+        # real-valued head weights and FP8 e4m3 queries/keys (DSA's indexer)
+        if t.get("w_idx_f") is not None:
+            a.w_idx_f = pks._dptr(t["w_idx_f"], torch.float32, "w_idx_f")
+        a.idx_fp8 = 1 if t.get("idx_fp8") else 0
         nbytes = pks.pks_decode_workspace_size(a)
         self.select_workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         a.workspace = self.select_workspace.data_ptr()
