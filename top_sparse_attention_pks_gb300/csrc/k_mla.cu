@@ -10,8 +10,10 @@
 // tcgen05 MMA with its accumulator in tensor memory is for.
 //
 // One CTA per (request, split of its selected tokens, half of the latent
-// value width).  Threads 0-127 are the 128 rows of the MMA (query heads, zero
-// rows above H; thread i owns tensor-memory lane i); warp 4 is the producer.
+// value width).  Threads 0-255 are the softmax threads, two per row of the MMA
+// (query heads, zero rows above H; row h is tensor-memory lane h, read by
+// warps h / 32 and h / 32 + 4, each for half of the row's columns); warp 8 is
+// the producer.
 // Per 64-token tile:
 //   S[128 x 64]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
 //   P             = exp2(S * scale - m)         one thread per head row
@@ -55,7 +57,8 @@ constexpr int kDK = kMlaLatent + kMlaRope;  // key width d + r
 constexpr int kTile = 64;                   // tokens per tile (MMA N of S)
 constexpr int kRows = 128;                  // MMA M: query heads, zero padded
 constexpr int kHalf = kDL / 2;              // value columns per CTA
-constexpr int kThreads = kRows + 32;   // 4 softmax warps + the producer warp
+constexpr int kCons = 2 * kRows;       // softmax threads: two per head row
+constexpr int kThreads = kCons + 32;   // 8 softmax warps + the producer warp
 constexpr int kBlk = kDK / 64;              // 64-value (128-byte) column blocks
 constexpr int kQTmemDims = 384;             // Q values 0..383 live in tensor memory
 constexpr int kQSmemBlk = (kDK - kQTmemDims) / 64;  // the rest: 3 column blocks in smem
@@ -246,11 +249,12 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   extern __shared__ uint8_t smem_raw[];
   // bar_rows[i]: tile rows of slot i published (producer); bar_s: S ready;
   // bar_p: P written (128 softmax threads); bar_o: O update done
-  __shared__ __align__(8) uint64_t bar_rows[2], bar_full[2], bar_s, bar_p, bar_o;
+  __shared__ __align__(8) uint64_t bar_rows[2], bar_full[2], bar_s, bar_p, bar_o, bar_mx, bar_ps;
   __shared__ uint32_t s_tmem;
   __shared__ int32_t s_row[3][kTile];
   __shared__ uint32_t s_mask[3][kTile / 32];
   __shared__ int s_abort;
+  __shared__ float s_mx[2][kRows], s_ps[2][kRows];  // a row's two halves: tile max, sum
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = blockIdx.x & 1;
@@ -274,10 +278,10 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   const int t_hi = (int)((int64_t)(split + 1) * ntiles_req / splits);
   const int ntiles = t_hi - t_lo;
   const int64_t slot = (int64_t)b * splits + split;  // partial slot of this CTA
-  const int h = tid;                                   // head row of a softmax thread
+  const int h = tid % kRows;                           // head row of a softmax thread
 
   if (ntiles == 0) {  // nothing selected in this range
-    if (h < H) {
+    if (tid < kRows && h < H) {
       if (splits > 1) {
         if (half == 0) part_ml[slot * H + h] = make_float2(kNegInf, 0.f);
       } else {
@@ -292,14 +296,16 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   const uint32_t sQ = base, sK = base + kQBytes, sP = sK + 2 * kKStageBytes;
 
   if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
-  if (tid == kRows) {
+  if (tid == kCons) {
     mbar_init(&bar_rows[0], 1);
     mbar_init(&bar_rows[1], 1);
-    mbar_init(&bar_full[0], kRows);
-    mbar_init(&bar_full[1], kRows);
+    mbar_init(&bar_full[0], kCons);
+    mbar_init(&bar_full[1], kCons);
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_p, kRows);
+    mbar_init(&bar_p, kCons);
     mbar_init(&bar_o, 1);
+    mbar_init(&bar_mx, kCons);
+    mbar_init(&bar_ps, kCons);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     s_abort = 0;
   }
@@ -356,7 +362,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   __syncthreads();
   tc_fence_after();
 
-  if (warp == kRows / 32) {
+  if (warp == kCons / 32) {
     // ================= producer warp: rows, K/V gathers, MMA issue =========
     // physical row of each position of tile `tile` (-1: none); lane handles
     // positions lane and lane + 32
@@ -459,8 +465,11 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       s_abort = 1;
     }
   } else {
-    // ================= softmax warps: one thread per head row ==============
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+    // ================= softmax warps: two threads per head row =============
+    // thread tid: row h = tid % 128 (warps w and w + 4 share TMEM lanes), half
+    // ch = tid / 128 of the row's S columns (32 of 64) and O columns (128 of 256)
+    const int ch = tid / kRows;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
     // every lane waits; a vote keeps control flow warp-uniform (the TMEM
     // accesses are warp-collective)
     auto waitw = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -474,7 +483,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       const int rs = tile % 3;
       const uint32_t dst0 = sK + (uint32_t)st * kKStageBytes;
 #pragma unroll 2
-      for (int id = tid; id < kTile * kBlk * 8; id += kRows) {
+      for (int id = tid; id < kTile * kBlk * 8; id += kCons) {
         const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
         const int j = cc >> 3, c = cc & 7;
         const int row = s_row[rs][r];
@@ -518,37 +527,50 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         break;
       }
       tc_fence_after();
-      const uint32_t mask0 = s_mask[t % 3][0], mask1 = s_mask[t % 3][1];
-      float sv[kTile];
-      tmem_ld32(tmem + lane_off + kTmemS, *reinterpret_cast<float(*)[32]>(&sv[0]));
-      tmem_ld32(tmem + lane_off + kTmemS + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-      float mt = kNegInf;
+      const uint32_t mask = s_mask[t % 3][ch];
+      float sv[32];
+      tmem_ld32(tmem + lane_off + kTmemS + ch * 32, sv);
+      float mh = kNegInf;
 #pragma unroll
-      for (int j = 0; j < kTile; ++j) {
-        const uint32_t mk = j < 32 ? mask0 : mask1;
-        sv[j] = (mk >> (j & 31)) & 1u ? sv[j] * scale_log2 : kNegInf;
-        mt = fmaxf(mt, sv[j]);
+      for (int j = 0; j < 32; ++j) {
+        sv[j] = (mask >> j) & 1u ? sv[j] * scale_log2 : kNegInf;
+        mh = fmaxf(mh, sv[j]);
       }
+      // the row's max over both halves (both threads get the same value)
+      s_mx[ch][h] = mh;
+      mbar_arrive(&bar_mx);
+      if (!waitw(&bar_mx, t & 1)) {
+        ok = false;
+        break;
+      }
+      const float mt = fmaxf(s_mx[0][h], s_mx[1][h]);
       const bool move = mt > m_run + 8.f;  // also true on the first valid tile
       const float m_new = move ? mt : m_run;
       const float alpha = move ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
-      float psum = 0.f;
-      uint32_t pk[kTile / 2];
+      float ph = 0.f;
+      uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < kTile; j += 2) {
+      for (int j = 0; j < 32; j += 2) {
         const float p0 = sv[j] == kNegInf ? 0.f : ex2_approx(sv[j] - m_new);
         const float p1 = sv[j + 1] == kNegInf ? 0.f : ex2_approx(sv[j + 1] - m_new);
         const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-        psum += __low2float(pp) + __high2float(pp);
+        ph += __low2float(pp) + __high2float(pp);
         pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pp);
       }
-      l_run = l_run * alpha + psum;
+      // the row's sum, added in the same order by both threads
+      s_ps[ch][h] = ph;
+      mbar_arrive(&bar_ps);
+      if (!waitw(&bar_ps, t & 1)) {
+        ok = false;
+        break;
+      }
+      l_run = l_run * alpha + (s_ps[0][h] + s_ps[1][h]);
       m_run = m_new;
       // rescale the O accumulated so far (warp-wide: TMEM access is collective)
       if (__any_sync(0xffffffffu, move && t > 0)) {
         const float a = (move && t > 0) ? alpha : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
+        for (int c = ch * 4; c < ch * 4 + 4; ++c) {  // this thread's 128 O columns
           float ov[32];
           tmem_ld32(tmem + lane_off + kTmemO + c * 32, ov);
 #pragma unroll
@@ -557,13 +579,14 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         }
       }
       // P row h: 64 bf16 = eight 16-byte chunks, 128-byte swizzle (chunk c of
-      // row h at chunk c ^ (h & 7))
+      // row h at chunk c ^ (h & 7)); this thread writes chunks 4ch .. 4ch + 3
       const uint32_t prow = sP + (uint32_t)h * 128;
 #pragma unroll
-      for (int c = 0; c < kTile / 8; ++c) {
+      for (int i = 0; i < 4; ++i) {
+        const int c = ch * 4 + i;
         const uint32_t dst = prow + ((c ^ (h & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(pk[4 * c]),
-                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(pk[4 * i]),
+                     "r"(pk[4 * i + 1]), "r"(pk[4 * i + 2]), "r"(pk[4 * i + 3])
                      : "memory");
       }
       fence_async_smem();
@@ -576,7 +599,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < kHalf / 32; ++c) {
+      for (int c = ch * 4; c < ch * 4 + 4; ++c) {
         float ov[32];
         tmem_ld32(tmem + lane_off + kTmemO + c * 32, ov);
         if (h < H) {
@@ -604,7 +627,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
           }
         }
       }
-      if (splits > 1 && half == 0 && h < H) part_ml[slot * H + h] = make_float2(m_run, l_run);
+      if (splits > 1 && half == 0 && ch == 0 && h < H)
+        part_ml[slot * H + h] = make_float2(m_run, l_run);
     } else {
       ok = false;
     }
