@@ -218,3 +218,43 @@ def test_dsa_step_fp8_indexer_real_weights_mla():
             unsel = np.setdiff1d(np.arange(n), sel)
             assert exact[b, sel].min() >= exact[b, unsel].max() - 1e-3 * np.abs(exact[b, :n]).max()
     check_attention(out, _oracle_mla(t, got, wl.page_size), "dsa step")
+
+
+@pytest.mark.parametrize("page_size", [1, 64])
+def test_mla_page_sizes(page_size):
+    lens = (403, 96, 241, 30, 176)
+    npages = sum(-(-n // page_size) for n in lens) + 3
+    wl = MLA_WORKLOADS["mla_paging_example"].replace(
+        page_size=page_size, num_pages=npages, max_pages=-(-max(lens) // page_size))
+    t = _prepare(wl)
+    rng = np.random.default_rng(page_size)
+    idx = _random_lists(rng, lens, 80)
+    att = MlaAttention(t["seq_lens"], t["block_table"], torch.from_numpy(idx).cuda(), t["q"],
+                       t["kv"])
+    out = att()
+    torch.cuda.synchronize()
+    assert att.device_error() == 0
+    check_attention(out, _oracle_mla(t, idx, page_size), f"page_size={page_size}")
+
+
+def test_mla_one_head_one_token_and_one_split():
+    wl = MLA_WORKLOADS["mla_paging_example"]
+    t = _prepare(wl)
+    q1 = t["q"][:, :1].contiguous()
+    idx = np.full((wl.B, 1), -1, np.int32)
+    idx[:, 0] = [5, 0, 240, 29, 100]
+    att = MlaAttention(t["seq_lens"], t["block_table"], torch.from_numpy(idx).cuda(), q1, t["kv"])
+    out = att()
+    torch.cuda.synchronize()
+    # one selected token: the output is its latent row (to bf16 rounding)
+    check_attention(out, _oracle_mla(t, idx, wl.page_size, q=q1), "one head, one token")
+    # every request's whole list in one CTA pair (splits = 1), 2048 positions
+    wl2 = MLA_WORKLOADS["mla_paging_example"].replace(seq_lens=(3000,), B=1, num_pages=200,
+                                                      max_pages=190)
+    t2 = _prepare(wl2)
+    idx2 = _random_lists(np.random.default_rng(3), [3000], 2048, holes=False)
+    att2 = MlaAttention(t2["seq_lens"], t2["block_table"], torch.from_numpy(idx2).cuda(), t2["q"],
+                        t2["kv"], splits=1)
+    out2 = att2()
+    torch.cuda.synchronize()
+    check_attention(out2, _oracle_mla(t2, idx2, wl2.page_size), "one split, 32 tiles")
