@@ -258,3 +258,21 @@ def test_mla_one_head_one_token_and_one_split():
     out2 = att2()
     torch.cuda.synchronize()
     check_attention(out2, _oracle_mla(t2, idx2, wl2.page_size), "one split, 32 tiles")
+
+
+def test_mla_more_ctas_than_sms():
+    """96 requests, one split each: 192 CTAs of 230 KB, so a second wave of
+    CTAs allocates tensor memory after the first wave has freed it."""
+    lens = tuple(int(x) for x in np.random.default_rng(9).integers(1, 300, size=96))
+    npages = sum(-(-n // 16) for n in lens)
+    wl = MLA_WORKLOADS["mla_paging_example"].replace(
+        B=96, seq_lens=lens, num_pages=npages, max_pages=-(-max(lens) // 16))
+    t = _prepare(wl)
+    idx = _random_lists(np.random.default_rng(10), lens, 128)
+    att = MlaAttention(t["seq_lens"], t["block_table"], torch.from_numpy(idx).cuda(), t["q"],
+                       t["kv"], splits=1)
+    for _ in range(2):
+        out = att()
+    torch.cuda.synchronize()
+    assert att.device_error() == 0
+    check_attention(out, _oracle_mla(t, idx, wl.page_size), "96 requests")
