@@ -16,7 +16,7 @@
 // the producer.
 // Per 64-token tile:
 //   S[128 x 64]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
-//   P             = exp2(S * scale - m)         one thread per head row
+//   P             = exp2(S * scale - m)         two threads per head row
 //   O[128 x 256] += P[128 x 64] . V[64 x 256]   tcgen05.mma, fp32 in TMEM
 // A tcgen05.mma costs about the same time for N = 32 or 64 and M = 64 or
 // 128 (measured), so S is computed 64 tokens at a time.  Tensor memory holds
@@ -37,8 +37,9 @@
 //     commit -> bar_o) and then S = Q.K^T of tile t once its gathers landed
 //     (bar_full, commit -> bar_s);
 //   softmax warps: after the O update of tile t - 1 (bar_o) gather tile t + 1
-//     into the freed stage, then take S of tile t (bar_s), write P, publish
-//     their gathers of tile t + 1 (bar_full) and P (bar_p).
+//     into the freed stage, then take S of tile t (bar_s), exchange each
+//     row's max and sum between its two threads (bar_mx, bar_ps), write P,
+//     publish their gathers of tile t + 1 (bar_full) and P (bar_p).
 // So the tensor pipe runs O(t - 1) before S(t) and a stage is refilled while
 // the other one is being multiplied.  With several splits per request the
 // CTAs write (m, l, O) partials that k_mla_merge combines.
@@ -57,8 +58,8 @@ constexpr int kDK = kMlaLatent + kMlaRope;  // key width d + r
 constexpr int kTile = 64;                   // tokens per tile (MMA N of S)
 constexpr int kRows = 128;                  // MMA M: query heads, zero padded
 constexpr int kHalf = kDL / 2;              // value columns per CTA
-constexpr int kCons = 2 * kRows;       // softmax threads: two per head row
-constexpr int kThreads = kCons + 32;   // 8 softmax warps + the producer warp
+constexpr int kCons = 2 * kRows;            // softmax threads: two per head row
+constexpr int kThreads = kCons + 32;        // 8 softmax warps + the producer warp
 constexpr int kBlk = kDK / 64;              // 64-value (128-byte) column blocks
 constexpr int kQTmemDims = 384;             // Q values 0..383 live in tensor memory
 constexpr int kQSmemBlk = (kDK - kQTmemDims) / 64;  // the rest: 3 column blocks in smem
@@ -477,7 +478,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
     };
     float m_run = kNegInf, l_run = 0.f;
     bool ok = true;
-    // gather tile `tile` into stage st: 32 rows x 72 16-byte chunks, 128-byte
+    // gather tile `tile` into stage st: 64 rows x 72 16-byte chunks, 128-byte
     // swizzle (chunk c of row r in column block j at chunk c ^ (r & 7))
     auto load_tile = [&](int tile, int st) {
       const int rs = tile % 3;
