@@ -258,6 +258,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   __shared__ float s_mx[2][kRows], s_ps[2][kRows];  // a row's two halves: tile max, sum
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the merge kernel may take SM slots now (it waits for this grid to finish)
+  pdl_launch_dependents();
   const int half = blockIdx.x & 1;
   const int split = (blockIdx.x >> 1) % splits;
   const int b = (blockIdx.x >> 1) / splits;
@@ -282,6 +284,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   const int h = tid % kRows;                           // head row of a softmax thread
 
   if (ntiles == 0) {  // nothing selected in this range
+    pdl_wait();  // the previous kernel may still read the outputs
     if (tid < kRows && h < H) {
       if (splits > 1) {
         if (half == 0) part_ml[slot * H + h] = make_float2(kNegInf, 0.f);
@@ -410,6 +413,9 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
     };
     bool ok = true;
+    // the selection comes from the top-k kernel: everything above (tensor
+    // memory, barriers, Q) overlapped its tail
+    pdl_wait();
     // rows of the first two tiles; the softmax warps gather a tile once its
     // rows are published on bar_rows
     resolve(t_lo, 0);
@@ -651,6 +657,7 @@ __global__ void __launch_bounds__(128)
 k_mla_merge(const float2* __restrict__ part_ml, const float* __restrict__ part_o,
             __nv_bfloat16* __restrict__ out, int H, int splits) {
   const int h = blockIdx.x, b = blockIdx.y;
+  pdl_wait();  // the partials come from k_mla_attention
   const float kNegInf = __int_as_float(0xff800000);
   float M = kNegInf;
   for (int s = 0; s < splits; ++s) {
@@ -719,18 +726,20 @@ cudaError_t launch_mla(const pks_mla_args& a, const MlaLayout& L, cudaStream_t s
   const float scale = a.sm_scale > 0.f ? a.sm_scale : 1.f / sqrtf((float)kDK);
   const float scale_log2 = scale * 1.4426950408889634f;
   const int grid = a.B * L.splits * 2;
-  k_mla_attention<<<grid, kThreads, kSmemBytes, s>>>(
-      a.seq_lens, a.block_table, static_cast<const __nv_bfloat16*>(a.q),
-      static_cast<const __nv_bfloat16*>(a.kv), a.topk_idx,
-      reinterpret_cast<float2*>(ws + L.part_ml), reinterpret_cast<float*>(ws + L.part_o),
-      static_cast<__nv_bfloat16*>(a.out), reinterpret_cast<int32_t*>(ws + L.err), a.B, a.H,
-      a.page_size, a.max_pages, a.num_pages, a.k, a.trim ? 1 : 0, L.splits, scale_log2);
-  e = cudaGetLastError();
+  // programmatic dependent launches: the MLA kernel's set-up overlaps the
+  // previous kernel (the top-k of the step), the merge's launch the MLA tail
+  e = launch_ex(k_mla_attention, dim3(grid), dim3(kThreads), kSmemBytes, s, /*pdl=*/true,
+                /*coop=*/false, a.seq_lens, a.block_table,
+                static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.kv),
+                a.topk_idx, reinterpret_cast<float2*>(ws + L.part_ml),
+                reinterpret_cast<float*>(ws + L.part_o), static_cast<__nv_bfloat16*>(a.out),
+                reinterpret_cast<int32_t*>(ws + L.err), a.B, a.H, a.page_size, a.max_pages,
+                a.num_pages, a.k, a.trim ? 1 : 0, L.splits, scale_log2);
   if (e != cudaSuccess || L.splits == 1) return e;
-  k_mla_merge<<<dim3(a.H, a.B), 128, 0, s>>>(reinterpret_cast<const float2*>(ws + L.part_ml),
-                                             reinterpret_cast<const float*>(ws + L.part_o),
-                                             static_cast<__nv_bfloat16*>(a.out), a.H, L.splits);
-  return cudaGetLastError();
+  return launch_ex(k_mla_merge, dim3(a.H, a.B), dim3(128), 0, s, /*pdl=*/true, /*coop=*/false,
+                   reinterpret_cast<const float2*>(ws + L.part_ml),
+                   reinterpret_cast<const float*>(ws + L.part_o),
+                   static_cast<__nv_bfloat16*>(a.out), a.H, L.splits);
 }
 
 }  // namespace pks
