@@ -260,9 +260,11 @@ def test_mla_one_head_one_token_and_one_split():
     check_attention(out2, _oracle_mla(t2, idx2, wl2.page_size), "one split, 32 tiles")
 
 
-def test_mla_more_ctas_than_sms():
-    """96 requests, one split each: 192 CTAs of 230 KB, so a second wave of
-    CTAs allocates tensor memory after the first wave has freed it."""
+@pytest.mark.parametrize("splits", [1, 2])
+def test_mla_more_ctas_than_sms(splits):
+    """96 requests, one or two splits each: 192 or 384 CTAs of 230 KB, so later
+    waves allocate tensor memory after earlier ones have freed it (with two
+    splits the merge kernel follows, launched as a programmatic dependent)."""
     lens = tuple(int(x) for x in np.random.default_rng(9).integers(1, 300, size=96))
     npages = sum(-(-n // 16) for n in lens)
     wl = MLA_WORKLOADS["mla_paging_example"].replace(
@@ -270,7 +272,7 @@ def test_mla_more_ctas_than_sms():
     t = _prepare(wl)
     idx = _random_lists(np.random.default_rng(10), lens, 128)
     att = MlaAttention(t["seq_lens"], t["block_table"], torch.from_numpy(idx).cuda(), t["q"],
-                       t["kv"], splits=1)
+                       t["kv"], splits=splits)
     for _ in range(2):
         out = att()
     torch.cuda.synchronize()
