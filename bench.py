@@ -352,10 +352,26 @@ def main():
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
 
+    if res is not None:
+        # the residency update (one CTA) needs only the selection: it runs on a
+        # side stream beside the attention, whose grid leaves one SM free for it
+        side = torch.cuda.Stream(device=dev)
+        ev_fork = torch.cuda.Event()
+        ev_join = torch.cuda.Event()
+        attn_args = pks.pks_decode_args.from_buffer_copy(step.args)
+        attn_args.attn_splits = torch.cuda.get_device_properties(dev).multi_processor_count - 1
+
     def one_step(stream):
-        step(stream)
-        if res is not None:
-            res.update(step.topk_idx, t["block_table"], wl.page_size, miss, n_miss, stream)
+        if res is None:
+            step(stream)
+            return
+        pks.pks_decode_select(step.args, stream)
+        ev_fork.record(stream)
+        side.wait_event(ev_fork)
+        res.update(step.topk_idx, t["block_table"], wl.page_size, miss, n_miss, side)
+        pks.pks_sparse_attention(attn_args, stream)
+        ev_join.record(side)
+        stream.wait_event(ev_join)
 
     with torch.cuda.stream(s):
         for _ in range(3):
