@@ -72,3 +72,37 @@ def test_empty_batch_launches_nothing():
     step()  # no device work, no error
     torch.cuda.synchronize()
     assert step.device_error() == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_real_weights_at_the_limits(fp8):
+    """fp32 keys (real head weights, and FP8 e4m3 inputs) through the largest k
+    and a 1.5M-token request: the selection is bit-exact against the oracle's
+    top-k on the kernel's own scores (and, with int8 inputs, on the oracle's)."""
+    import oracle
+    from top_sparse_attention_pks_gb300.workloads import draw_float_weights, draw_fp8_indexer
+    n = 1_500_000
+    wl = WORKLOADS["paging_example"].replace(
+        B=3, seq_lens=(n, 70000, 1000), k=65536, page_size=64, max_pages=-(-n // 64),
+        num_pages=-(-n // 64) + 1200 + 20, Di=64, D=64, Hq=4, Hkv=1, Hi=2)
+    t, _, _ = prepare(wl)
+    if fp8:
+        t["q_idx"], t["idx_k"] = draw_fp8_indexer(wl, "cuda")
+        t["idx_fp8"] = True
+    t["w_idx_f"] = draw_float_weights(wl, "cuda", signed=True)
+    step = SparseDecodeStep(t, wl.k)
+    _, idx = step()
+    torch.cuda.synchronize()
+    assert step.device_error() == 0
+    lens = host(t["seq_lens"]).numpy()
+    got_sc = pks.float_key_to_score(host(step.scores()).numpy())
+    got = host(idx).numpy()
+    np.testing.assert_array_equal(got, oracle.topk_f(lens, got_sc, wl.k))
+    if not fp8:
+        ref_sc = oracle.indexer_scores_f(lens, host(t["block_table"]).numpy(), wl.page_size,
+                                         host(t["q_idx"]).numpy(), host(t["w_idx_f"]).numpy(),
+                                         host(t["idx_k"]).numpy())
+        for b, m in enumerate(lens):
+            np.testing.assert_array_equal(got_sc[b, :m], ref_sc[b, :m])
+    del t, step
+    torch.cuda.empty_cache()
