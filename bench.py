@@ -8,7 +8,8 @@ cached token, exact top-k, paged sparse attention (plus the residency update
 for the workload with an HBM slot table).  Default workload: 16 requests x
 131072 tokens, 64-token pages, GQA 64/8, head dim 128, 4-head int8 indexer,
 top-2048.  Inputs are seeded synthetic tensors resident in HBM; L2 is flushed
-(256 MB write) between timed steps, outside the timed intervals.
+(256 MB write, then 256 MB read of another buffer) between timed steps,
+outside the timed intervals.
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own
 replica batch (weak scaling, no collective on the data path).
@@ -43,6 +44,22 @@ METRIC = "sparse decode steps/s"
 UNIT = "steps/s"
 NOMINAL_HBM_GBS = 8000.0  # the roofline denominator the target is stated against
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: a 256 MB write (twice the 129 MB L2),
+    then a 256 MB read of a second buffer.  The read writes back the dirty
+    lines the write leaves, so the next step starts with an L2 that holds
+    none of its inputs and nothing to write back (a write alone leaves up to
+    129 MB of dirty lines whose write-back lands inside the next step)."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 def measured_peaks():
@@ -348,7 +365,7 @@ def main():
                                  device=dev)
         miss = torch.empty(wl.num_pages, dtype=torch.int32, device=dev)
         n_miss = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
 
@@ -388,7 +405,7 @@ def main():
 
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             g.replay()
     torch.cuda.synchronize()
     topk_host = step.topk_idx.cpu().numpy()
@@ -406,7 +423,7 @@ def main():
     time.sleep(0.3)  # let the sampler start before the work
     with torch.cuda.stream(s):
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             starts[i].record(s)
             g.replay()
             ends[i].record(s)
@@ -430,10 +447,10 @@ def main():
         en2 = [torch.cuda.Event(enable_timing=True) for _ in range(n2)]
         with torch.cuda.stream(s):
             for _ in range(args.warmup):
-                flush.zero_()
+                flush()
                 g2.replay()
             for i in range(n2):
-                flush.zero_()
+                flush()
                 st2[i].record(s)
                 g2.replay()
                 en2[i].record(s)
@@ -451,7 +468,7 @@ def main():
             for e in row:
                 e.record(s)
         for i in range(args.stage_steps):
-            flush.zero_()
+            flush()
             step.timed(evs[i], s)
     torch.cuda.synchronize()
     for e in evs:
@@ -629,7 +646,7 @@ def mla_bench(wl, args, dev, rank, world, dist):
               flush=True)
         return
     step = MlaDecodeStep(t, wl.k)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -646,7 +663,7 @@ def mla_bench(wl, args, dev, rank, world, dist):
     mla_launches = 1 + (1 if pks.pks_mla_workspace_size(step.attention.args) > 256 else 0)
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             g.replay()
     torch.cuda.synchronize()
     ab = mla_algorithmic(wl, h["seq_lens"].numpy(), bt, step.topk_idx.cpu().numpy())
@@ -661,7 +678,7 @@ def mla_bench(wl, args, dev, rank, world, dist):
     time.sleep(0.3)
     with torch.cuda.stream(s):
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             starts[i].record(s)
             g.replay()
             ends[i].record(s)
@@ -681,7 +698,7 @@ def mla_bench(wl, args, dev, rank, world, dist):
             for e in row:
                 e.record(s)
         for i in range(n_st):
-            flush.zero_()
+            flush()
             evs[i][0].record(s)
             step.select(s)
             evs[i][1].record(s)
@@ -745,7 +762,7 @@ def mla_bench(wl, args, dev, rank, world, dist):
     tot = 0.0
     with torch.cuda.stream(s):
         for i in range(n + 3):
-            flush.zero_()
+            flush()
             s.synchronize()
             t0 = time.perf_counter()
             ge.replay()
@@ -793,7 +810,7 @@ def hisparse_bench(wl, t, h, args, dev, rank):
                             h["initial_resident"].numpy())
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     page_bytes = host_k[0].numel() * host_k.element_size()
     # a decode step brings a new indexer query: cycle through 8 seeded ones
     # (copied into place before each step, outside the timed interval)
@@ -812,7 +829,7 @@ def hisparse_bench(wl, t, h, args, dev, rank):
     for i in range(n):
         with torch.cuda.stream(s):
             t["q_idx"].copy_(q_var[(args.warmup + i) % 8])
-            flush.zero_()
+            flush()
             e = ev[i]
             e[0].record(s)
             pks.pks_decode_select(rs.args, s)
@@ -847,7 +864,7 @@ def hisparse_bench(wl, t, h, args, dev, rank):
                           "attention": med[3]},
             "fetch": {"pages_per_step": fetch_pages, "bytes_per_step": fetch_bytes,
                       "gbs": fetch_bytes / (med[2] * 1e-3) / 1e9},
-            "timing": "CUDA events between the four calls, L2 write-flushed before each step",
+            "timing": "CUDA events between the four calls, L2 flushed (256 MB write + 256 MB read) before each step",
             "queries": "a new seeded indexer query each step (8 in rotation)",
         }), flush=True)
 
@@ -890,7 +907,7 @@ def config_dict(wl, args):
                                 else "float32 [B, Hi] U[0.25,2)")
             if getattr(args, "float_weights", False) else "int32 [Hi] (ones)",
             "residency_slots": wl.capacity, "parallelism": f"replicas x{args.gpus}",
-            "l2": "flushed between timed steps (256 MB write, outside the timed intervals)",
+            "l2": "flushed between timed steps (256 MB write, then 256 MB read of another buffer; outside the timed intervals)",
             "timing": "CUDA events around each CUDA-graph replay of the step"}
 
 
@@ -959,7 +976,7 @@ def end_to_end(step, t, wl, args, s, flush, res, miss, n_miss):
     total = 0.0
     with torch.cuda.stream(s):
         for i in range(n + 3):
-            flush.zero_()
+            flush()
             s.synchronize()
             t0 = time.perf_counter()
             g.replay()
