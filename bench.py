@@ -746,12 +746,10 @@ def mla_bench(wl, args, dev, rank, world, dist):
     n = max(1, min(args.steps, args.e2e_steps))
 
     def call():  # the calls a user makes for one step
-        for nm in names:
-            t[nm].copy_(host_in[nm], non_blocking=True)
+        pks.pks_stage_copy([(t[nm], host_in[nm]) for nm in names], s)
         pks.pks_decode_select(step.select_args, s)
         pks.pks_mla_sparse_attention(step.attention.args, s)
-        out_h.copy_(step.out, non_blocking=True)
-        idx_h.copy_(step.topk_idx, non_blocking=True)
+        pks.pks_stage_copy([(out_h, step.out), (idx_h, step.topk_idx)], s)
 
     with torch.cuda.stream(s):
         call()
@@ -771,8 +769,8 @@ def mla_bench(wl, args, dev, rank, world, dist):
                 tot += time.perf_counter() - t0
     e2e = {"value": n / tot, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": n, "timing": "host wall clock per step: one CUDA-graph replay of the step's "
-                                 "calls (copies in from pinned memory, select, MLA, copies out) "
-                                 "and a stream synchronise"}
+                                 "calls (pks_stage_copy in from pinned memory, select, MLA, "
+                                 "pks_stage_copy out) and a stream synchronise"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -941,8 +939,9 @@ def profiled_traffic(kernel, workload):
 
 def end_to_end(step, t, wl, args, s, flush, res, miss, n_miss):
     """Per step: pinned host -> device copy of the step's inputs (queries,
-    lengths, block table), the public pks_decode_step call, device -> pinned
-    host copy of the outputs (attention output, top-k), host synchronise."""
+    lengths, block table; one pks_stage_copy), the public pks_decode_step
+    call, device -> pinned host copy of the outputs (attention output, top-k;
+    one pks_stage_copy), host synchronise."""
     names = ["q", "q_idx", "seq_lens", "block_table"]
     host_in = {n: t[n].cpu().pin_memory() for n in names}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
@@ -956,14 +955,15 @@ def end_to_end(step, t, wl, args, s, flush, res, miss, n_miss):
     n = max(1, min(args.steps, args.e2e_steps))
 
     def call():  # the calls a user makes for one step
-        for nm in names:
-            t[nm].copy_(host_in[nm], non_blocking=True)
+        # inputs in and outputs out with one staging launch each (SM loads and
+        # stores over the CPU-GPU link)
+        pks.pks_stage_copy([(t[nm], host_in[nm]) for nm in names], s)
         pks.pks_decode_step(step.args, s)
+        outs = [(out_h, step.out), (idx_h, step.topk_idx)]
         if res is not None:
             res.update(step.topk_idx, t["block_table"], wl.page_size, miss, n_miss, s)
-            extra[0].copy_(n_miss, non_blocking=True)
-        out_h.copy_(step.out, non_blocking=True)
-        idx_h.copy_(step.topk_idx, non_blocking=True)
+            outs.append((extra[0], n_miss))
+        pks.pks_stage_copy(outs, s)
 
     # captured once (copies from and to the pinned host buffers included),
     # replayed per step: one launch from the host instead of ten calls
@@ -986,8 +986,9 @@ def end_to_end(step, t, wl, args, s, flush, res, miss, n_miss):
     return {"value": n / total, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n,
             "timing": "host wall clock per step: one CUDA-graph replay of the step's calls "
-                      "(host-to-device copies from pinned memory, pks_decode_step, "
-                      "device-to-host copies of output and top-k) and a stream synchronise"}
+                      "(pks_stage_copy of the inputs from pinned memory, pks_decode_step, "
+                      "pks_stage_copy of output and top-k to pinned memory) and a stream "
+                      "synchronise"}
 
 
 if __name__ == "__main__":

@@ -392,6 +392,34 @@ pks_status pks_mla_sparse_attention(const pks_mla_args* args, pks_stream stream)
  * Synchronises the stream. */
 pks_status pks_mla_device_error(const pks_mla_args* args, int32_t* code, pks_stream stream);
 
+/* ---- staging of a step's inputs and outputs --------------------------------
+ * Not an operation of the pages: a serving convenience for moving a step's
+ * small inputs (queries, lengths, block table) in and its outputs (attention
+ * output, top-k) out.  On a GB300 the SMs load and store page-locked host
+ * memory over the CPU-GPU link faster than the copy engines move buffers of
+ * this size, and one launch replaces one copy per buffer. */
+
+/* At most this many ranges per pks_stage_copy call. */
+#define PKS_STAGE_MAX_RANGES 8
+
+/* One byte range: dst and src are device memory or page-locked host memory
+ * that the device can address (cudaHostAlloc / cudaMallocHost / registered
+ * memory on a unified-address system).  Ranges of one call must not overlap. */
+typedef struct pks_copy_range {
+  void* dst;
+  const void* src;
+  size_t bytes;
+} pks_copy_range;
+
+/* Copy n (1..PKS_STAGE_MAX_RANGES) byte ranges with one kernel launch on
+ * `stream`: 16-byte loads and stores where dst, src and bytes are all
+ * multiples of 16, bytes otherwise.  `ranges` is a host array, read before
+ * the call returns (the kernel gets the ranges as arguments, so the call can
+ * be captured into a CUDA graph).  Zero-byte ranges are allowed; a null dst
+ * or src with bytes > 0, n out of range or ranges null: INVALID, nothing is
+ * enqueued.  Ordered like any kernel on the stream. */
+pks_status pks_stage_copy(const pks_copy_range* ranges, int32_t n, pks_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -237,3 +237,21 @@ def test_mla_workspace_and_validation_without_gpu():
     # null device pointers with B > 0
     a = _mla_cpu_args()
     assert L.pks_mla_sparse_attention(ctypes.byref(a), None) == -1
+
+
+def test_stage_copy_argument_errors():
+    # rejected on the host, before any launch
+    INVALID = -1
+    L = pks.lib()
+    R = pks.pks_copy_range
+    arr = (R * 9)()
+    for i in range(9):
+        arr[i] = R(16, 32, 16)
+    assert L.pks_stage_copy(None, 1, None) == INVALID
+    assert L.pks_stage_copy(arr, 0, None) == INVALID
+    assert L.pks_stage_copy(arr, pks.PKS_STAGE_MAX_RANGES + 1, None) == INVALID
+    arr[1] = R(None, 32, 16)
+    assert L.pks_stage_copy(arr, 2, None) == INVALID
+    arr[1] = R(16, None, 16)
+    assert L.pks_stage_copy(arr, 2, None) == INVALID
+    assert pks.PKS_STAGE_MAX_RANGES == 8

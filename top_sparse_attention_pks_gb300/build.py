@@ -24,7 +24,7 @@ LIB = LIBDIR / "libpks.so"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["pks_host.cpp", "k_indexer.cu", "k_topk.cu", "k_attention.cu", "k_residency.cu",
-           "k_mla.cu"]
+           "k_mla.cu", "k_stage.cu"]
 
 
 def nvcc() -> str:

@@ -689,4 +689,12 @@ pks_status pks_mla_device_error(const pks_mla_args* args, int32_t* code, pks_str
   return PKS_OK;
 }
 
+pks_status pks_stage_copy(const pks_copy_range* ranges, int32_t n, pks_stream stream) {
+  if (!ranges || n < 1 || n > PKS_STAGE_MAX_RANGES) return PKS_ERR_INVALID;
+  for (int i = 0; i < n; ++i)
+    if (ranges[i].bytes > 0 && (!ranges[i].dst || !ranges[i].src)) return PKS_ERR_INVALID;
+  return pks::from_cuda(
+      pks::launch_stage_copy(ranges, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -142,6 +142,10 @@ cudaError_t launch_residency_fetch(const int32_t* page_slot, const int32_t* miss
                                    const uint8_t* host_v, uint8_t* slot_k, uint8_t* slot_v,
                                    int64_t page_bytes, int num_pages, int capacity,
                                    cudaStream_t s);
+// Staging copy of up to kStageMaxRanges byte ranges in one launch (k_stage.cu);
+// the ranges are validated by the caller.
+constexpr int kStageMaxRanges = PKS_STAGE_MAX_RANGES;
+cudaError_t launch_stage_copy(const pks_copy_range* ranges, int n, cudaStream_t s);
 // ---- sparse MLA in MQA mode (tcgen05 kernel in k_mla.cu)
 constexpr int kMlaLatent = 512;  // d: latent width, the value
 constexpr int kMlaRope = 64;     // r: RoPE part of the key

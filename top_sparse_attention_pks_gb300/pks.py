@@ -83,6 +83,12 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+class pks_copy_range(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
+PKS_STAGE_MAX_RANGES = 8
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _ST = ctypes.c_int32
@@ -139,7 +145,8 @@ def _declare(L):
     L.pks_residency_update.argtypes = [_P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P,
                                        _P]
     L.pks_residency_update.restype = _ST
-
+    L.pks_stage_copy.argtypes = [ctypes.POINTER(pks_copy_range), _I32, _P]
+    L.pks_stage_copy.restype = _ST
 
     _PM = ctypes.POINTER(pks_mla_args)
     L.pks_mla_workspace_size.argtypes = [_PM, ctypes.POINTER(ctypes.c_size_t)]
@@ -380,6 +387,28 @@ def pks_residency_fetch(state: torch.Tensor, num_pages: int, capacity: int,
         _dptr(host_k, torch.bfloat16, "host_k"), _dptr(host_v, torch.bfloat16, "host_v"),
         _dptr(slot_k, torch.bfloat16, "slot_k"), _dptr(slot_v, torch.bfloat16, "slot_v"),
         int(page_bytes), _stream(stream)), "pks_residency_fetch")
+
+
+def pks_stage_copy(pairs: Sequence, stream=None) -> None:
+    """One launch copying each (dst, src) pair of equally sized tensors (device
+    or page-locked host memory), in order of the pairs; at most
+    PKS_STAGE_MAX_RANGES pairs."""
+    n = len(pairs)
+    arr = (pks_copy_range * max(1, n))()
+    for i, (dst, src) in enumerate(pairs):
+        nb = dst.numel() * dst.element_size()
+        if src.numel() * src.element_size() != nb:
+            raise ValueError(f"pks_stage_copy: pair {i} sizes differ")
+        if nb == 0:  # nothing to move (empty tensors are never page-locked)
+            arr[i] = pks_copy_range(None, None, 0)
+            continue
+        if not (dst.is_contiguous() and src.is_contiguous()):
+            raise ValueError(f"pks_stage_copy: pair {i} not contiguous")
+        if (dst.device.type == "cpu" and not dst.is_pinned()) or \
+                (src.device.type == "cpu" and not src.is_pinned()):
+            raise ValueError(f"pks_stage_copy: pair {i} host tensor not page-locked")
+        arr[i] = pks_copy_range(dst.data_ptr(), src.data_ptr(), nb)
+    _check(lib().pks_stage_copy(arr, n, _stream(stream)), "pks_stage_copy")
 
 
 def pks_decode_step(args: pks_decode_args, stream=None) -> None:
