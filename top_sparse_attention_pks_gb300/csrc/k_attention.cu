@@ -487,6 +487,7 @@ k_attention_merge(const int32_t* __restrict__ prefix, const float2* __restrict__
   const int lane = threadIdx.x & 31;
   const int qh = blockIdx.x * 4 + (threadIdx.x >> 5);  // query head
   const int b = blockIdx.y;
+  pdl_launch_dependents();  // a following kernel may launch and wait for this grid
   pdl_wait();  // prefix and partials come from the attention kernel
   if (qh >= Hq) return;
   const int h = qh / G, gg = qh % G;  // KV head and row within its group

@@ -145,6 +145,9 @@ k_indexer_scan_mma(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   extern __shared__ int smem_i[];
   // the top-k grid may take SM slots as soon as this grid's CTAs retire
   pdl_launch_dependents();
+  // launched with programmatic serialization: inputs staged by the kernel
+  // before this one (if any) are visible after the wait
+  pdl_wait();
   int* s_hist = smem_i;                      // [NQ][kScoreBins]
   int* s_prefix = smem_i + NQ * kScoreBins;  // [B + 1]
   // NQ > 1 or FW: (weighted) ReLU of each (token, query head) of a warp's round
@@ -441,11 +444,9 @@ cudaError_t launch_scan_t(const pks_decode_args& a, int32_t* scores, int64_t ld,
   auto kern = k_indexer_scan_mma<HI, DI, kMmaThreads, NQ, FW, F8>;
   cudaError_t e = raise_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
-  kern<<<device_sm_count(), kMmaThreads, smem, s>>>(a.seq_lens, a.block_table, a.q_idx, a.w_idx,
-                                                    a.w_idx_f, a.idx_k, scores, ld, hist, err, a.B,
-                                                    a.max_pages, a.page_size, shift, a.num_pages,
-                                                    a.k);
-  return cudaGetLastError();
+  return launch_ex(kern, dim3(device_sm_count()), dim3(kMmaThreads), smem, s, /*pdl=*/true,
+                   /*coop=*/false, a.seq_lens, a.block_table, a.q_idx, a.w_idx, a.w_idx_f, a.idx_k,
+                   scores, ld, hist, err, a.B, a.max_pages, a.page_size, shift, a.num_pages, a.k);
 }
 
 }  // namespace

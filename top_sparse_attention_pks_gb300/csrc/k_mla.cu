@@ -657,6 +657,7 @@ __global__ void __launch_bounds__(128)
 k_mla_merge(const float2* __restrict__ part_ml, const float* __restrict__ part_o,
             __nv_bfloat16* __restrict__ out, int H, int splits) {
   const int h = blockIdx.x, b = blockIdx.y;
+  pdl_launch_dependents();  // a following kernel may launch and wait for this grid
   pdl_wait();  // the partials come from k_mla_attention
   const float kNegInf = __int_as_float(0xff800000);
   float M = kNegInf;

@@ -36,6 +36,10 @@ __device__ __forceinline__ int range_of(const StageRanges& r, int64_t u) {
 
 __global__ void __launch_bounds__(kStageThreads)
 k_stage_copy(const StageRanges r) {
+  // launched with programmatic serialization: the next kernel may launch now
+  // and wait for this one; this one waits for the kernel before it
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * kStageThreads;
   for (int64_t u0 = (int64_t)blockIdx.x * kStageThreads + threadIdx.x; u0 < r.total;
        u0 += stride * kStageUnroll) {
@@ -91,8 +95,8 @@ cudaError_t launch_stage_copy(const pks_copy_range* ranges, int n, cudaStream_t 
   int64_t grid = (total + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (grid > cap) grid = cap;
-  k_stage_copy<<<(unsigned)grid, kStageThreads, 0, s>>>(r);
-  return cudaGetLastError();
+  return launch_ex(k_stage_copy, dim3((unsigned)grid), dim3(kStageThreads), 0, s, /*pdl=*/true,
+                   /*coop=*/false, r);
 }
 
 }  // namespace pks
