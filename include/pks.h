@@ -367,7 +367,9 @@ typedef struct pks_mla_args {
                                   after (the decode step's own top-k), so only the first
                                   min(k, len_b) positions are visited; 0: all k */
   int32_t splits;              /* CTA pairs per request: 0 = automatic (one pair per two
-                                  SMs spread over the requests), else 1..64 */
+                                  SMs spread over the requests), else 1..64; raised to
+                                  ceil(ceil(k / 64) / 32) when lower (a CTA takes at most
+                                  32 tiles of 64 tokens) */
   int32_t reserved[1];         /* must be 0 */
 } pks_mla_args;
 

@@ -10,10 +10,10 @@
 // tcgen05 MMA with its accumulator in tensor memory is for.
 //
 // One CTA per (request, split of its selected tokens, half of the latent
-// value width).  Threads 0-255 are the softmax threads, two per row of the MMA
-// (query heads, zero rows above H; row h is tensor-memory lane h, read by
-// warps h / 32 and h / 32 + 4, each for half of the row's columns); warp 8 is
-// the producer.
+// value width), 512 threads: warps 0-7 are the softmax threads, two per row of
+// the MMA (query heads, zero rows above H; row h is tensor-memory lane h, read
+// by warps h / 32 and h / 32 + 4, each for half of the row's columns); warp 8
+// is the producer (MMA issue); warps 9-15 gather the K/V rows.
 // Per 64-token tile:
 //   S[128 x 64]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
 //   P             = exp2(S * scale - m)         two threads per head row
@@ -32,17 +32,19 @@
 // TMEM.
 //
 // Roles and hand-offs (mbarriers, every wait bounded):
-//   producer warp: resolves the rows of tile t + 2 through the block table
-//     (bar_rows), issues O += P.V of tile t - 1 once its P is written (bar_p,
-//     commit -> bar_o) and then S = Q.K^T of tile t once its gathers landed
-//     (bar_full, commit -> bar_s);
-//   softmax warps: after the O update of tile t - 1 (bar_o) gather tile t + 1
-//     into the freed stage, then take S of tile t (bar_s), exchange each
-//     row's max and sum between its two threads (bar_mx, bar_ps), write P,
-//     publish their gathers of tile t + 1 (bar_full) and P (bar_p).
-// So the tensor pipe runs O(t - 1) before S(t) and a stage is refilled while
-// the other one is being multiplied.  With several splits per request the
-// CTAs write (m, l, O) partials that k_mla_merge combines.
+//   all threads, once: the physical row of every position of the CTA's tiles
+//     (top-k entry, then block table) into a shared table;
+//   gather warps: tile t into stage t & 1 once the O update of tile t - 2 has
+//     released the stage (bar_free), then publish it (bar_full);
+//   producer warp: issues O += P.V of tile t - 1 once its P is written (bar_p,
+//     commit -> bar_o and bar_free) and then S = Q.K^T of tile t once its
+//     gathers landed (bar_full, commit -> bar_s);
+//   softmax warps: after the O update of tile t - 1 (bar_o) take S of tile t
+//     (bar_s), exchange each row's max and sum between its two threads
+//     (bar_mx, bar_ps), rescale O if the max moved, write P (bar_p).
+// So the tensor pipe runs O(t - 1) before S(t), and the next tile's gathers
+// run beside the softmax instead of in front of it.  With several splits per
+// request the CTAs write (m, l, O) partials that k_mla_merge combines.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -59,7 +61,9 @@ constexpr int kTile = 64;                   // tokens per tile (MMA N of S)
 constexpr int kRows = 128;                  // MMA M: query heads, zero padded
 constexpr int kHalf = kDL / 2;              // value columns per CTA
 constexpr int kCons = 2 * kRows;            // softmax threads: two per head row
-constexpr int kThreads = kCons + 32;        // 8 softmax warps + the producer warp
+constexpr int kProdWarp = kCons / 32;       // warp 8: the producer
+constexpr int kGather = 224;                 // gather threads: warps 9-15 (512 threads a CTA)
+constexpr int kThreads = kCons + 32 + kGather;  // softmax, producer, gather warps
 constexpr int kBlk = kDK / 64;              // 64-value (128-byte) column blocks
 constexpr int kQTmemDims = 384;             // Q values 0..383 live in tensor memory
 constexpr int kQSmemBlk = (kDK - kQTmemDims) / 64;  // the rest: 3 column blocks in smem
@@ -74,6 +78,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = kHalf, kTmemQ = kHalf + kTile;
 static_assert(kTmemQ + kQTmemDims / 2 == kTmemCols, "O, S and Q fill the tensor memory");
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
+// tiles of one CTA whose rows are resolved up front (the host picks enough
+// splits that no CTA has more)
+constexpr int kMaxCtaTiles = kMlaMaxCtaTiles;
 
 static_assert(kDK % 64 == 0 && kDL % 64 == 0, "latent and key widths in 64-value blocks");
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
@@ -248,12 +255,14 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
                 int32_t* __restrict__ err, int B, int H, int page_size, int max_pages,
                 int num_pages, int k, int trim, int splits, float scale_log2) {
   extern __shared__ uint8_t smem_raw[];
-  // bar_rows[i]: tile rows of slot i published (producer); bar_s: S ready;
+  // bar_full[i]: stage i gathered (gather warps); bar_s: S ready;
   // bar_p: P written (128 softmax threads); bar_o: O update done
-  __shared__ __align__(8) uint64_t bar_rows[2], bar_full[2], bar_s, bar_p, bar_o, bar_mx, bar_ps;
+  // bar_free[i]: the O update of the last tile in stage i is done (the stage
+  // may be refilled)
+  __shared__ __align__(8) uint64_t bar_full[2], bar_free[2], bar_s, bar_p, bar_o, bar_mx, bar_ps;
   __shared__ uint32_t s_tmem;
-  __shared__ int32_t s_row[3][kTile];
-  __shared__ uint32_t s_mask[3][kTile / 32];
+  __shared__ int32_t s_row[kMaxCtaTiles][kTile];         // physical row of each position
+  __shared__ uint32_t s_mask[kMaxCtaTiles][kTile / 32];  // positions with a row
   __shared__ int s_abort;
   __shared__ float s_mx[2][kRows], s_ps[2][kRows];  // a row's two halves: tile max, sum
 
@@ -283,6 +292,10 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   const int64_t slot = (int64_t)b * splits + split;  // partial slot of this CTA
   const int h = tid % kRows;                           // head row of a softmax thread
 
+  if (ntiles > kMaxCtaTiles) {  // more than the row table holds: the host rules this out
+    if (tid == 0) flag_error(err, kErrState);
+    return;
+  }
   if (ntiles == 0) {  // nothing selected in this range
     pdl_wait();  // the previous kernel may still read the outputs
     if (tid < kRows && h < H) {
@@ -301,10 +314,10 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
 
   if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
   if (tid == kCons) {
-    mbar_init(&bar_rows[0], 1);
-    mbar_init(&bar_rows[1], 1);
-    mbar_init(&bar_full[0], kCons);
-    mbar_init(&bar_full[1], kCons);
+    mbar_init(&bar_full[0], kGather);
+    mbar_init(&bar_full[1], kGather);
+    mbar_init(&bar_free[0], 1);
+    mbar_init(&bar_free[1], 1);
     mbar_init(&bar_s, 1);
     mbar_init(&bar_p, kCons);
     mbar_init(&bar_o, 1);
@@ -361,39 +374,39 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       tmem_st32(tmem + lo + kTmemQ + c * 32, v);
     }
   }
-  // the staging area becomes the K stages: every thread is done reading it
+  // the selection comes from the top-k kernel: everything above (tensor
+  // memory, barriers, Q) overlapped its tail.  Then every thread helps to
+  // resolve the physical row of each position of this CTA's tiles (-1: none),
+  // one 32-position group a warp at a time
+  pdl_wait();
+  for (int g = warp; g < ntiles * (kTile / 32); g += kThreads / 32) {
+    const int tile = g / (kTile / 32), w = g % (kTile / 32);
+    const int p = (t_lo + tile) * kTile + w * 32 + lane;
+    int row = -1;
+    if (p < npos) {
+      const int t = topk[(int64_t)b * k + p];
+      if (t >= 0) {
+        if (t >= len) {
+          flag_error(err, kErrToken);
+        } else {
+          const int page = block_table[(int64_t)b * max_pages + t / page_size];
+          if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
+          else flag_error(err, kErrPage);
+        }
+      }
+    }
+    s_row[tile][w * 32 + lane] = row;
+    const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
+    if (lane == 0) s_mask[tile][w] = m;
+  }
+  // the staging area becomes the K stages: every thread is done reading it,
+  // and the rows are in place
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  if (warp == kCons / 32) {
-    // ================= producer warp: rows, K/V gathers, MMA issue =========
-    // physical row of each position of tile `tile` (-1: none); lane handles
-    // positions lane and lane + 32
-    auto resolve = [&](int tile, int rs) {
-#pragma unroll
-      for (int w = 0; w < kTile / 32; ++w) {
-        const int pos = w * 32 + lane;
-        const int p = tile * kTile + pos;
-        int row = -1;
-        if (tile < t_hi && p < npos) {
-          const int t = topk[(int64_t)b * k + p];
-          if (t >= 0) {
-            if (t >= len) {
-              flag_error(err, kErrToken);
-            } else {
-              const int page = block_table[(int64_t)b * max_pages + t / page_size];
-              if ((unsigned)page < (unsigned)num_pages) row = page * page_size + t % page_size;
-              else flag_error(err, kErrPage);
-            }
-          }
-        }
-        s_row[rs][pos] = row;
-        const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
-        if (lane == 0) s_mask[rs][w] = m;
-      }
-      __syncwarp();
-    };
+  if (warp == kProdWarp) {
+    // ================= producer warp: MMA issue =============================
     const uint64_t dq0 = smem_desc(sQ, 16, 1024, kSw128);
     const uint64_t dp0 = smem_desc(sP, 16, 1024, kSw128);
     auto issue_pv = [&](int tt) {  // O += P . V(tile tt)
@@ -405,6 +418,24 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         mma_bf16(tmem + kTmemO, dp0 + (uint64_t)((kk * 32) >> 4),
                  dv0 + (uint64_t)((kk * 16 * 128) >> 4), kIdescO, (tt > 0 || kk > 0) ? 1u : 0u);
       mma_commit(&bar_o);
+      mma_commit(&bar_free[tt & 1]);
+    };
+    // S = Q . K^T of local tile tt into the S accumulator (one thread)
+    auto issue_s = [&](int tt) {
+      const uint64_t dk0 = smem_desc(sK + (uint32_t)(tt & 1) * kKStageBytes, 16, 1024, kSw128);
+#pragma unroll
+      for (int kk = 0; kk < kDK / 16; ++kk) {
+        const uint64_t db = dk0 + (uint64_t)(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4);
+        if (kk < kQTmemDims / 16) {
+          mma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + kk * 8, db, kIdescS, kk > 0 ? 1u : 0u);
+        } else {
+          const int qk = kk - kQTmemDims / 16;
+          mma_bf16(tmem + kTmemS,
+                   dq0 + (uint64_t)(((qk >> 2) * kQBlockBytes + (qk & 3) * 32) >> 4), db,
+                   kIdescS, 1u);
+        }
+      }
+      mma_commit(&bar_s);
     };
     // lane 0 waits, the warp follows: control flow stays warp-uniform
     auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -413,18 +444,10 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
     };
     bool ok = true;
-    // the selection comes from the top-k kernel: everything above (tensor
-    // memory, barriers, Q) overlapped its tail
-    pdl_wait();
-    // rows of the first two tiles; the softmax warps gather a tile once its
-    // rows are published on bar_rows
-    resolve(t_lo, 0);
-    if (lane == 0) mbar_arrive(&bar_rows[0]);
-    resolve(t_lo + 1, 1);
-    if (lane == 0) mbar_arrive(&bar_rows[1]);
     for (int t = 0; t < ntiles && ok; ++t) {
-      // 1. the previous tile's O update, as soon as its P is written (it
-      //    also frees that tile's stage and the S accumulator)
+      // 1. the previous tile's O update, as soon as its P is written (its
+      //    completion frees P, the S accumulator's reader and, on bar_free,
+      //    the previous tile's stage for the gather warps)
       if (t > 0) {
         if (!wait0(&bar_p, (t - 1) & 1)) { ok = false; break; }
         if (lane == 0) {
@@ -433,32 +456,13 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         }
         __syncwarp();
       }
-      // 2. S = Q . K^T of this tile once the softmax warps' gathers landed
+      // 2. S = Q . K^T of this tile once the gather warps' copies landed
       if (!wait0(&bar_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
       if (lane == 0) {
         tc_fence_after();
-        const uint64_t dk0 = smem_desc(sK + (uint32_t)(t & 1) * kKStageBytes, 16, 1024, kSw128);
-#pragma unroll
-        for (int kk = 0; kk < kDK / 16; ++kk) {
-          const uint64_t db = dk0 + (uint64_t)(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4);
-          if (kk < kQTmemDims / 16) {
-            mma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + kk * 8, db, kIdescS, kk > 0 ? 1u : 0u);
-          } else {
-            const int qk = kk - kQTmemDims / 16;
-            mma_bf16(tmem + kTmemS,
-                     dq0 + (uint64_t)(((qk >> 2) * kQBlockBytes + (qk & 3) * 32) >> 4), db,
-                     kIdescS, 1u);
-          }
-        }
-        mma_commit(&bar_s);
+        issue_s(t);
       }
       __syncwarp();
-      // 3. rows of the tile after next (its slot was last read by the
-      //    softmax warps for tile t - 1, which have written its P)
-      if (t + 2 < ntiles) {
-        resolve(t_lo + t + 2, (t + 2) % 3);
-        if (lane == 0) mbar_arrive(&bar_rows[t & 1]);
-      }
     }
     if (ok) {
       if (!wait0(&bar_p, (ntiles - 1) & 1)) ok = false;
@@ -471,7 +475,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       flag_error(err, kErrTimeout);
       s_abort = 1;
     }
-  } else {
+  } else if (warp < kProdWarp) {
     // ================= softmax warps: two threads per head row =============
     // thread tid: row h = tid % 128 (warps w and w + 4 share TMEM lanes), half
     // ch = tid / 128 of the row's S columns (32 of 64) and O columns (128 of 256)
@@ -484,36 +488,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
     };
     float m_run = kNegInf, l_run = 0.f;
     bool ok = true;
-    // gather tile `tile` into stage st: 64 rows x 72 16-byte chunks, 128-byte
-    // swizzle (chunk c of row r in column block j at chunk c ^ (r & 7))
-    auto load_tile = [&](int tile, int st) {
-      const int rs = tile % 3;
-      const uint32_t dst0 = sK + (uint32_t)st * kKStageBytes;
-#pragma unroll 2
-      for (int id = tid; id < kTile * kBlk * 8; id += kCons) {
-        const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
-        const int j = cc >> 3, c = cc & 7;
-        const int row = s_row[rs][r];
-        const __nv_bfloat16* src = kv + (row >= 0 ? (int64_t)row * kDK + cc * 8 : 0);
-        cp_async16(dst0 + j * kKBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src,
-                   row >= 0 ? 16 : 0);
-      }
-      cp_async_commit();
-    };
-    // this thread's gathers of a tile have landed: make them visible to the
-    // tensor core and count them on the stage's barrier
-    auto publish = [&](int st) {
-      cp_async_wait_all();
-      fence_async_smem();
-      mbar_arrive(&bar_full[st]);
-    };
-    if (!waitw(&bar_rows[0], 0)) ok = false;
-    if (ok) {
-      load_tile(0, 0);
-      publish(0);
-    }
     for (int t = 0; t < ntiles && ok; ++t) {
-      // the O update of tile t - 1 has read its stage (the next tile's) and P
+      // the O update of tile t - 1 is done: O may be rescaled and P rewritten
       if (t > 0) {
         if (!waitw(&bar_o, (t - 1) & 1)) {
           ok = false;
@@ -521,20 +497,12 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         }
         tc_fence_after();
       }
-      const bool next = t + 1 < ntiles;
-      if (next) {
-        if (!waitw(&bar_rows[(t + 1) & 1], ((t + 1) >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        load_tile(t + 1, (t + 1) & 1);
-      }
       if (!waitw(&bar_s, t & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t mask = s_mask[t % 3][ch];
+      const uint32_t mask = s_mask[t][ch];
       float sv[32];
       tmem_ld32(tmem + lane_off + kTmemS + ch * 32, sv);
       float mh = kNegInf;
@@ -598,7 +566,6 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       }
       fence_async_smem();
       tc_fence_before();
-      if (next) publish((t + 1) & 1);
       mbar_arrive(&bar_p);
     }
     // ---- O of this CTA's half: to the output, or to the partial slot
@@ -638,6 +605,41 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         part_ml[slot * H + h] = make_float2(m_run, l_run);
     } else {
       ok = false;
+    }
+    if (!ok && lane == 0) {
+      flag_error(err, kErrTimeout);
+      s_abort = 1;
+    }
+  } else {
+    // ================= gather warps: K/V rows of every tile =================
+    // tile t goes to stage t & 1 once the O update of tile t - 2 (the stage's
+    // last reader) is done; its 64 rows x 72 16-byte chunks, 128-byte swizzle
+    // (chunk c of row r in column block j at chunk c ^ (r & 7))
+    const int gt = tid - (kCons + 32);
+    bool ok = true;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int st = t & 1;
+      if (t >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar_free[st], ((t - 2) >> 1) & 1, &s_abort))) {
+          ok = false;
+          break;
+        }
+      }
+      const uint32_t dst0 = sK + (uint32_t)st * kKStageBytes;
+#pragma unroll 2
+      for (int id = gt; id < kTile * kBlk * 8; id += kGather) {
+        const int r = id / (kBlk * 8), cc = id % (kBlk * 8);
+        const int j = cc >> 3, c = cc & 7;
+        const int row = s_row[t][r];
+        const __nv_bfloat16* src = kv + (row >= 0 ? (int64_t)row * kDK + cc * 8 : 0);
+        cp_async16(dst0 + j * kKBlockBytes + r * 128 + ((c ^ (r & 7)) << 4), src,
+                   row >= 0 ? 16 : 0);
+      }
+      cp_async_commit();
+      // this thread's copies have landed: visible to the tensor core, counted
+      cp_async_wait_all();
+      fence_async_smem();
+      mbar_arrive(&bar_full[st]);
     }
     if (!ok && lane == 0) {
       flag_error(err, kErrTimeout);
@@ -688,11 +690,16 @@ k_mla_merge(const float2* __restrict__ part_ml, const float* __restrict__ part_o
 }  // namespace
 
 int mla_splits(const pks_mla_args& a) {
-  if (a.splits > 0) return a.splits;
   const int tiles = (a.k + kTile - 1) / kTile;
-  const int per = a.B > 0 ? device_sm_count() / (2 * a.B) : 1;
-  int s = per < 1 ? 1 : per;
-  if (s > tiles) s = tiles;
+  // no CTA takes more tiles than its row table holds
+  const int least = (tiles + kMaxCtaTiles - 1) / kMaxCtaTiles;
+  int s = a.splits;
+  if (s <= 0) {
+    const int per = a.B > 0 ? device_sm_count() / (2 * a.B) : 1;
+    s = per < 1 ? 1 : per;
+    if (s > tiles) s = tiles;
+  }
+  if (s < least) s = least;
   return s < 1 ? 1 : s;
 }
 

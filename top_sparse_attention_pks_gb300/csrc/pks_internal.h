@@ -150,6 +150,9 @@ cudaError_t launch_stage_copy(const pks_copy_range* ranges, int n, cudaStream_t 
 constexpr int kMlaLatent = 512;  // d: latent width, the value
 constexpr int kMlaRope = 64;     // r: RoPE part of the key
 constexpr int kMlaMaxSplits = 64;
+// Most 64-token tiles one MLA CTA takes (its rows are resolved up front):
+// the split count is raised until ceil(ceil(k / 64) / splits) fits.
+constexpr int kMlaMaxCtaTiles = 32;
 struct MlaLayout {
   int splits;
   size_t err, part_ml, part_o, total;
