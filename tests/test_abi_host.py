@@ -239,6 +239,24 @@ def test_mla_workspace_and_validation_without_gpu():
     assert L.pks_mla_sparse_attention(ctypes.byref(a), None) == -1
 
 
+def test_mla_split_count_keeps_each_cta_within_32_tiles():
+    # k = 4096: 64 tiles of 64 tokens; one split would give a CTA 64 tiles, so
+    # the library raises it to two (the workspace then holds two splits'
+    # partials, exactly as with splits = 2); k = 2048 keeps one split (no
+    # partials at all)
+    import ctypes
+    L = pks.lib()
+    n = ctypes.c_size_t()
+    sizes = {}
+    for k, splits in [(4096, 1), (4096, 2), (4096, 3), (2048, 1)]:
+        assert L.pks_mla_workspace_size(ctypes.byref(_mla_cpu_args(k=k, splits=splits)),
+                                        ctypes.byref(n)) == 0
+        sizes[(k, splits)] = n.value
+    assert sizes[(4096, 1)] == sizes[(4096, 2)]
+    assert sizes[(4096, 3)] > sizes[(4096, 2)]
+    assert sizes[(2048, 1)] < sizes[(4096, 2)]
+
+
 def test_stage_copy_argument_errors():
     # rejected on the host, before any launch
     INVALID = -1

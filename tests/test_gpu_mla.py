@@ -97,7 +97,7 @@ def test_mla_random_lists(H, splits):
 
 
 def test_mla_long_lists_many_tiles_and_scale():
-    """k = 2048 positions in 64 tiles over 2 splits; a non-default softmax scale
+    """k = 2048 positions in 32 tiles over 2 splits; a non-default softmax scale
     large enough that the running max moves several times (O rescaled in TMEM)."""
     wl = MLA_WORKLOADS["mla_paging_example"].replace(seq_lens=(3000, 2500), B=2, num_pages=400,
                                                      max_pages=200)
@@ -112,6 +112,23 @@ def test_mla_long_lists_many_tiles_and_scale():
         torch.cuda.synchronize()
         ref = _oracle_mla(t, idx, wl.page_size, scale=scale or None)
         check_attention(out, ref, f"scale={scale}")
+
+
+def test_mla_more_tiles_than_one_cta_holds():
+    """k = 4096 positions (64 tiles) with splits = 1: the library raises the
+    split count so that no CTA takes more than 32 tiles, and the partials of
+    the raised splits are merged as usual."""
+    wl = MLA_WORKLOADS["mla_paging_example"].replace(seq_lens=(5000, 4500), B=2, num_pages=700,
+                                                     max_pages=320)
+    t = _prepare(wl)
+    rng = np.random.default_rng(8)
+    idx = _random_lists(rng, [5000, 4500], 4096)
+    idx_d = torch.from_numpy(idx).cuda()
+    att = MlaAttention(t["seq_lens"], t["block_table"], idx_d, t["q"], t["kv"], splits=1)
+    out = att()
+    torch.cuda.synchronize()
+    assert att.device_error() == 0
+    check_attention(out, _oracle_mla(t, idx, wl.page_size), "k = 4096, splits 1 -> 2")
 
 
 def test_mla_decode_step_paging_example():
