@@ -250,8 +250,12 @@ pks_status pks_sparse_attention(const pks_decode_args* args, pks_stream stream);
  * same call.
  *
  * Set-up: the first call on each device looks up the array's address with
- * cudaGetSymbolAddress (that device current) and configures the kernels'
- * shared-memory limits; make that first call outside any stream capture.
+ * cudaGetSymbolAddress (that device current).  The attention kernel's
+ * shared-memory limit is shared with pks_sparse_attention and only ever
+ * raised: a call whose shapes need more shared memory than any earlier call
+ * of either entry point on the device raises it first.  Neither step is a
+ * stream operation; make the first call, and any call with a larger batch
+ * than before, outside stream capture.
  * The array is shared by every call on a device: calls that overlap in time
  * (other streams, concurrent graph replays, other host threads) race on it.
  * Device-side bounds checks skip bad rows as in pks_sparse_attention but are

@@ -88,3 +88,37 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
     pks.pks_sparse_attention_static(args_ok)
     torch.cuda.synchronize()
     _compare(step.out, before, "after rejection")
+
+
+def test_static_call_with_smaller_batch_keeps_workspace_path_working():
+    """The two entry points share one attention kernel and its shared-memory
+    limit, which grows with the batch.  A static call with a smaller batch
+    between two workspace calls with a larger one must not lower that limit:
+    the second workspace call has to launch and match the oracle."""
+    wl = WORKLOADS["b32_4k"].replace(B=6, seq_lens=(4096, 3000, 4096, 17, 2500, 4096),
+                                     num_pages=512)
+    t, _, _ = prepare(wl)
+    step = SparseDecodeStep(t, wl.k)
+    step()  # workspace path at B = 6
+    torch.cuda.synchronize()
+    idx = step.topk_idx.cpu().numpy()
+    ref = oracle_attention(wl, t, idx)
+    check_attention(step.out, ref, "workspace call before the static one")
+
+    wl1 = wl.replace(B=1, seq_lens=(4096,))
+    t1, _, _ = prepare(wl1)
+    step1 = SparseDecodeStep(t1, wl1.k)
+    step1()
+    torch.cuda.synchronize()
+    out1 = torch.full_like(step1.out, float("nan"))
+    args1 = pks.make_args(k=wl1.k, topk_idx=step1.topk_idx, out=out1, **t1)
+    pks.pks_sparse_attention_static(args1)  # same D and head group, smaller batch
+    torch.cuda.synchronize()
+    check_attention(out1, oracle_attention(wl1, t1, step1.topk_idx.cpu().numpy()),
+                    "static call with one request")
+
+    step.out.fill_(float("nan"))
+    step()  # workspace path at B = 6 again: the limit it needs is still set
+    torch.cuda.synchronize()
+    assert (step.topk_idx.cpu().numpy() == idx).all()
+    check_attention(step.out, ref, "workspace call after the static one")

@@ -569,6 +569,35 @@ size_t attn_smem_bytes(int B) {
          sizeof(int32_t) * (size_t)(kAttnRowCap + B + 1);
 }
 
+// Dynamic shared-memory limit of one attention instantiation on the current
+// device, raised to `smem` when it is lower and never lowered, with the
+// resident CTAs an SM it allows at that limit (cached with it).  Every
+// launcher of the instantiation goes through here, so a call with a small
+// batch cannot undo the limit that a larger one set.  Attribute calls are not
+// stream operations: after the first call at a size they stay out of any
+// graph capture.
+template <int D, int HG, bool RES>
+cudaError_t attn_configure(size_t smem, int* blocks_per_sm) {
+  static size_t configured[64] = {0};
+  static int per_sm[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > configured[dev]) {
+    auto kern = k_sparse_attention<D, HG, RES>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int bps = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, HG * 32, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
+    per_sm[dev] = bps < 1 ? 1 : bps;
+  }
+  *blocks_per_sm = per_sm[dev];
+  return cudaSuccess;
+}
+
 template <int D, int HG, bool RES>
 cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
                           bool trim, const ResidentKv& rk, cudaStream_t s) {
@@ -576,23 +605,12 @@ cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, ui
   const int nq = query_count(a);
   const int Bv = a.B * nq;  // virtual requests
   const size_t smem = attn_smem_bytes<D, HG>(Bv);
-  // raise the dynamic shared-memory limit once per device and size (not a
-  // stream operation, so it stays out of any graph capture after the first call)
-  static size_t configured[64] = {0};
-  static int per_sm[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  size_t& done = configured[dev & 63];
-  if (smem > done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int bps = 1;
+  {
+    cudaError_t e = attn_configure<D, HG, RES>(smem, &bps);
     if (e != cudaSuccess) return e;
-    done = smem;
-    int bps = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, HG * 32, smem);
-    per_sm[dev & 63] = bps < 1 ? 1 : bps;
   }
-  int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * per_sm[dev & 63];
+  int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * bps;
   if (grid > L.attn_grid_max) grid = L.attn_grid_max;
   const int G = a.Hq / a.Hkv;
   const int min_per_cta = a.attn_splits > 0 ? 0 : kAttnMinPositions;
@@ -653,14 +671,11 @@ cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cud
   const int nq = query_count(a);
   const int Bv = a.B * nq;
   const size_t smem = attn_smem_bytes<D, HG>(Bv);
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int bps = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, HG * 32, smem);
+  int bps = 1;
+  cudaError_t e = attn_configure<D, HG, false>(smem, &bps);
   if (e != cudaSuccess) return e;
   // the same grid pks_sparse_attention uses for these arguments
-  int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * (bps < 1 ? 1 : bps);
+  int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * bps;
   if (grid > kAttnGridMax) grid = kAttnGridMax;
   const StaticAttnLayout L = static_attn_layout(a, grid);
   if (L.total > kAttnStaticScratchBytes) {
