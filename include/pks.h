@@ -187,7 +187,10 @@ typedef struct pks_decode_args {
                              head's dot product is taken on the tensor core with fp32
                              accumulation in the hardware's order, then weighted and summed
                              over the heads as for w_idx_f */
-  int32_t reserved2;      /* must be 0 */
+  int32_t wait_limit;     /* polls of the top-k request barrier (a bounded device-side wait)
+                             before it gives up with device error 5: 0 = the default, 2^22
+                             (about half a second); >= 0 (INVALID otherwise).  Small values
+                             exist to exercise the time-out path */
 } pks_decode_args;
 
 /* Workspace bytes a step with these shapes needs (pointers may be NULL). */
@@ -261,6 +264,14 @@ pks_status pks_sparse_attention(const pks_decode_args* args, pks_stream stream);
  * Device-side bounds checks skip bad rows as in pks_sparse_attention but are
  * not reported (their flag lives in the array). */
 pks_status pks_sparse_attention_static(const pks_decode_args* args, pks_stream stream);
+
+/* Byte offset inside the workspace of the top-k request barriers' arrival
+ * counters (int32, one per request and query token, zero between steps), for
+ * diagnosis and for tests that make a barrier wait run out: a counter that
+ * starts below zero needs more arrivals than the request's CTAs make, so its
+ * CTAs give up after wait_limit polls with device error 5.  Host only;
+ * pointers in args may be NULL.  INVALID: bad shapes or offset NULL. */
+pks_status pks_decode_barrier_offset(const pks_decode_args* args, size_t* offset);
 
 /* Copy the workspace's device error word to *code (host) and clear it;
  * synchronises the stream.  *code = 0 when no device check fired, else the
@@ -374,7 +385,11 @@ typedef struct pks_mla_args {
                                   SMs spread over the requests), else 1..64; raised to
                                   ceil(ceil(k / 64) / 32) when lower (a CTA takes at most
                                   32 tiles of 64 tokens) */
-  int32_t reserved[1];         /* must be 0 */
+  int32_t wait_limit;          /* clock cycles a bounded mbarrier wait of the MLA kernel spins
+                                  before it gives up with device error 5 (the CTA's other
+                                  warps then stop too): 0 = the default, 4e9 (about 2 s);
+                                  >= 0 (INVALID otherwise).  Small values exist to exercise
+                                  the time-out path */
 } pks_mla_args;
 
 /* Workspace bytes pks_mla_sparse_attention needs for these shapes (pointers

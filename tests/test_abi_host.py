@@ -166,7 +166,7 @@ def test_workspace_size_and_validation_without_gpu():
     # no workspace -> PKS_ERR_WORKSPACE, before any device work
     assert L.pks_decode_step(ctypes.byref(a), None) == -7
     cases = [dict(Hq=6, Hkv=4), dict(k=0), dict(page_size=0), dict(B=-1),
-             dict(reserved=(ctypes.c_int32 * 1)(1)), dict(topk_mode=2), dict(topk_mode=-1), dict(n_queries=-1), dict(attn_splits=-2),
+             dict(reserved=(ctypes.c_int32 * 1)(1)), dict(wait_limit=-1), dict(topk_mode=2), dict(topk_mode=-1), dict(n_queries=-1), dict(attn_splits=-2),
              dict(attn_splits=1025)]
     for c in cases:
         assert L.pks_decode_workspace_size(ctypes.byref(_cpu_args(**c)),
@@ -230,7 +230,7 @@ def test_mla_workspace_and_validation_without_gpu():
     # no workspace -> PKS_ERR_WORKSPACE, before any device work
     assert L.pks_mla_sparse_attention(ctypes.byref(_mla_cpu_args(B=0, splits=2)), None) == -7
     for c in [dict(H=0), dict(H=129), dict(k=0), dict(B=-1), dict(splits=65), dict(trim=2),
-              dict(sm_scale=-1.0), dict(reserved=(ctypes.c_int32 * 1)(3)), dict(page_size=0)]:
+              dict(sm_scale=-1.0), dict(wait_limit=-1), dict(page_size=0)]:
         assert L.pks_mla_workspace_size(ctypes.byref(_mla_cpu_args(**c)), ctypes.byref(n)) == -1, c
     for c in [dict(d_latent=256), dict(d_rope=32)]:
         assert L.pks_mla_workspace_size(ctypes.byref(_mla_cpu_args(**c)), ctypes.byref(n)) == -6, c
@@ -273,3 +273,17 @@ def test_stage_copy_argument_errors():
     arr[1] = R(16, None, 16)
     assert L.pks_stage_copy(arr, 2, None) == INVALID
     assert pks.PKS_STAGE_MAX_RANGES == 8
+
+
+def test_barrier_offset_lies_in_the_control_block():
+    import ctypes
+    a = _cpu_args()
+    total = pks.pks_decode_workspace_size(a)
+    off = pks.pks_decode_barrier_offset(a)
+    assert off % 256 == 0 and 0 < off < total
+    # the counters follow the per-request score histograms (2048 int32 each)
+    assert off >= 2048 * 4 * a.B
+    L = pks.lib()
+    assert L.pks_decode_barrier_offset(ctypes.byref(a), None) == -1
+    assert L.pks_decode_barrier_offset(ctypes.byref(_cpu_args(k=0)),
+                                       ctypes.byref(ctypes.c_size_t())) == -1

@@ -77,7 +77,7 @@ constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: O (fp32), S (fp32), Q values 0..383 (two bf16 a column)
 constexpr uint32_t kTmemO = 0, kTmemS = kHalf, kTmemQ = kHalf + kTile;
 static_assert(kTmemQ + kQTmemDims / 2 == kTmemCols, "O, S and Q fill the tensor memory");
-constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
+constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz, unless wait_limit is set
 // tiles of one CTA whose rows are resolved up front (the host picks enough
 // splits that no CTA has more)
 constexpr int kMaxCtaTiles = kMlaMaxCtaTiles;
@@ -124,11 +124,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // bounded wait for the phase with the given parity; false when it gave up
 // or when another warp of the CTA has given up (*abort set)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort) {
+                                          const volatile int* abort, long long budget) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (*abort || clock64() - t0 > kWaitCycles) return false;
+    if (*abort || clock64() - t0 > budget) return false;
   return true;
+}
+// bounded wait that ignores the abort flag: the producer waits for its own
+// MMAs to complete before the tensor memory they write is freed
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return;
 }
 
 // ---- tcgen05: tensor memory, MMA, commit ----------------------------------
@@ -253,7 +260,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
                 const int32_t* __restrict__ topk, float2* __restrict__ part_ml,
                 float* __restrict__ part_o, __nv_bfloat16* __restrict__ out,
                 int32_t* __restrict__ err, int B, int H, int page_size, int max_pages,
-                int num_pages, int k, int trim, int splits, float scale_log2) {
+                int num_pages, int k, int trim, int splits, float scale_log2,
+                long long budget) {
   extern __shared__ uint8_t smem_raw[];
   // bar_full[i]: stage i gathered (gather warps); bar_s: S ready;
   // bar_p: P written (128 softmax threads); bar_o: O update done
@@ -439,11 +447,12 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
     };
     // lane 0 waits, the warp follows: control flow stays warp-uniform
     auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
-      bool w = lane == 0 ? mbar_wait(bar, parity, &s_abort) : true;
+      bool w = lane == 0 ? mbar_wait(bar, parity, &s_abort, budget) : true;
       __syncwarp();
       return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
     };
     bool ok = true;
+    int last_s = -1, last_pv = -1;  // the last tiles whose S / O update was issued
     for (int t = 0; t < ntiles && ok; ++t) {
       // 1. the previous tile's O update, as soon as its P is written (its
       //    completion frees P, the S accumulator's reader and, on bar_free,
@@ -453,6 +462,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         if (lane == 0) {
           tc_fence_after();
           issue_pv(t - 1);
+          last_pv = t - 1;
         }
         __syncwarp();
       }
@@ -461,6 +471,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       if (lane == 0) {
         tc_fence_after();
         issue_s(t);
+        last_s = t;
       }
       __syncwarp();
     }
@@ -469,12 +480,20 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       else if (lane == 0) {
         tc_fence_after();
         issue_pv(ntiles - 1);
+        last_pv = ntiles - 1;
       }
     }
     if (!ok && lane == 0) {
       flag_error(err, kErrTimeout);
       s_abort = 1;
     }
+    // every MMA issued above completes before the tensor memory is freed,
+    // also when another warp gave up (normally these have completed already)
+    if (lane == 0) {
+      if (last_s >= 0) mbar_drain(&bar_s, last_s & 1);
+      if (last_pv >= 0) mbar_drain(&bar_o, last_pv & 1);
+    }
+    __syncwarp();
   } else if (warp < kProdWarp) {
     // ================= softmax warps: two threads per head row =============
     // thread tid: row h = tid % 128 (warps w and w + 4 share TMEM lanes), half
@@ -484,7 +503,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
     // every lane waits; a vote keeps control flow warp-uniform (the TMEM
     // accesses are warp-collective)
     auto waitw = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &s_abort)) != 0;
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &s_abort, budget)) != 0;
     };
     float m_run = kNegInf, l_run = 0.f;
     bool ok = true;
@@ -620,7 +639,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
     for (int t = 0; t < ntiles && ok; ++t) {
       const int st = t & 1;
       if (t >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar_free[st], ((t - 2) >> 1) & 1, &s_abort))) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&bar_free[st], ((t - 2) >> 1) & 1, &s_abort, budget))) {
           ok = false;
           break;
         }
@@ -742,7 +762,8 @@ cudaError_t launch_mla(const pks_mla_args& a, const MlaLayout& L, cudaStream_t s
                 a.topk_idx, reinterpret_cast<float2*>(ws + L.part_ml),
                 reinterpret_cast<float*>(ws + L.part_o), static_cast<__nv_bfloat16*>(a.out),
                 reinterpret_cast<int32_t*>(ws + L.err), a.B, a.H, a.page_size, a.max_pages,
-                a.num_pages, a.k, a.trim ? 1 : 0, L.splits, scale_log2);
+                a.num_pages, a.k, a.trim ? 1 : 0, L.splits, scale_log2,
+                a.wait_limit > 0 ? (long long)a.wait_limit : kWaitCycles);
   if (e != cudaSuccess || L.splits == 1) return e;
   return launch_ex(k_mla_merge, dim3(a.H, a.B), dim3(128), 0, s, /*pdl=*/true, /*coop=*/false,
                    reinterpret_cast<const float2*>(ws + L.part_ml),

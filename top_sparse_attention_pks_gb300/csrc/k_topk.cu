@@ -40,7 +40,8 @@ constexpr int kPerThread = kTopkChunk / kTopkThreads;
 constexpr int kCandCap = 2048;
 // requests up to this many tokens are emitted through the shared bitmap
 constexpr int kBitmapTokens = 131072;
-// polls of a request barrier before it gives up (about 0.4 s)
+// polls of a request barrier before it gives up (about 0.4 s), unless the
+// caller sets wait_limit
 constexpr int kBarrierSpins = 1 << 22;
 
 __device__ __forceinline__ int score_bin(int s) {
@@ -246,8 +247,8 @@ __device__ __forceinline__ void request_arrive(int32_t* arrive) {
 }
 
 // Bounded wait until `count` CTAs of a request have arrived (one thread).
-__device__ __forceinline__ bool request_wait(int32_t* arrive, int count) {
-  for (int it = 0; it < kBarrierSpins; ++it) {
+__device__ __forceinline__ bool request_wait(int32_t* arrive, int count, int spins) {
+  for (int it = 0; it < spins; ++it) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(arrive) : "memory");
     if (v >= count) {
@@ -444,7 +445,7 @@ __device__ __forceinline__ uint64_t select_threshold(int n, int need, KeyAt key_
 __global__ void __launch_bounds__(kTopkThreads, 4)
 k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ scores,
               int64_t ld, TopkWs w, int2* __restrict__ chunk_cnt, int32_t* __restrict__ topk,
-              int k, int max_len, int nchunks_max, int nq) {
+              int k, int max_len, int nchunks_max, int nq, int spins) {
   __shared__ uint64_t s_key[kCandCap];
   __shared__ int s_eqoff[kTopkCoopMaxChunks + 1];  // candidates before each chunk
   __shared__ int s_before, s_lo, s_hi;
@@ -555,7 +556,7 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
   // ---- barrier of the request's CTAs
   __syncthreads();
   if (tid == 0) request_arrive(w.tick + b);
-  if (tid == 0) sm.flag = request_wait(w.tick + b, nch);
+  if (tid == 0) sm.flag = request_wait(w.tick + b, nch, spins);
   __syncthreads();
   if (!sm.flag) {
     if (tid == 0) atomicCAS(w.err, 0, kErrTimeout);
@@ -937,7 +938,8 @@ cudaError_t launch_topk(const pks_decode_args& a, const WorkspaceLayout& L, uint
     // that cannot all be resident
     return launch_ex(k_topk_select, grid, dim3(kTopkThreads), 0, s, /*pdl=*/true, /*coop=*/true,
                      a.seq_lens, scores, L.ld, w, reinterpret_cast<int2*>(ws + L.chunk_cnt),
-                     a.topk_idx, a.k, max_len, (int)L.nchunks, nq);
+                     a.topk_idx, a.k, max_len, (int)L.nchunks, nq,
+                     a.wait_limit > 0 ? a.wait_limit : kBarrierSpins);
   }
   const size_t smem = sizeof(uint64_t) * kCandCap + kBitmapTokens / 8 + sizeof(int) * L.nchunks;
   static size_t configured[64] = {0};

@@ -56,7 +56,7 @@ pks_status check_shapes(const pks_decode_args* a) {
   if ((nq & (nq - 1)) != 0 || (int64_t)a->Hi * nq > 8) return PKS_ERR_UNSUPPORTED;
   if ((int64_t)a->B * query_count(*a) > kMaxB) return PKS_ERR_UNSUPPORTED;
   if (a->w_idx_f && nq > 1) return PKS_ERR_UNSUPPORTED;  // real weights: one query token
-  if (a->idx_fp8 < 0 || a->idx_fp8 > 1 || a->reserved2 != 0) return PKS_ERR_INVALID;
+  if (a->idx_fp8 < 0 || a->idx_fp8 > 1 || a->wait_limit < 0) return PKS_ERR_INVALID;
   if (a->idx_fp8 && !a->w_idx_f) return PKS_ERR_INVALID;  // FP8 scores need real weights
   if ((int64_t)a->num_pages * a->page_size > INT32_MAX) return PKS_ERR_UNSUPPORTED;
   if (a->D != 64 && a->D != 128) return PKS_ERR_UNSUPPORTED;
@@ -450,6 +450,14 @@ pks_status pks_sparse_attention_static(const pks_decode_args* args, pks_stream s
   return too_large ? PKS_ERR_TOO_LARGE : PKS_OK;
 }
 
+pks_status pks_decode_barrier_offset(const pks_decode_args* args, size_t* offset) {
+  if (!offset) return PKS_ERR_INVALID;
+  const pks_status st = pks::check_shapes(args);
+  if (st != PKS_OK) return st;
+  *offset = pks::workspace_layout(*args).tick_topk;
+  return PKS_OK;
+}
+
 pks_status pks_decode_device_error(const pks_decode_args* args, int32_t* code,
                                    pks_stream stream) {
   if (!code) return PKS_ERR_INVALID;
@@ -632,7 +640,7 @@ pks_status mla_check(const pks_mla_args* a) {
   if (a->B < 0 || a->B > pks::kMaxB || a->H < 1 || a->H > 128 || a->page_size < 1 ||
       a->max_pages < 1 || a->num_pages < 1 || a->k < 1 || a->k > pks::kMaxK ||
       a->splits < 0 || a->splits > pks::kMlaMaxSplits || a->trim < 0 || a->trim > 1 ||
-      a->reserved[0] != 0 || !(a->sm_scale >= 0.f))
+      a->wait_limit < 0 || !(a->sm_scale >= 0.f))
     return PKS_ERR_INVALID;
   if (a->d_latent != pks::kMlaLatent || a->d_rope != pks::kMlaRope) return PKS_ERR_UNSUPPORTED;
   if ((int64_t)a->num_pages * a->page_size > INT32_MAX) return PKS_ERR_UNSUPPORTED;

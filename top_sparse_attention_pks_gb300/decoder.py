@@ -16,7 +16,7 @@ class SparseDecodeStep:
     """
 
     def __init__(self, tensors: dict, k: int, attn_splits: int = 0, topk_mode: int = 0,
-                 stream=None):
+                 stream=None, wait_limit: int = 0):
         t = dict(tensors)
         q = t["q"]
         dev = q.device
@@ -26,14 +26,15 @@ class SparseDecodeStep:
         self.out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         self.topk_idx = torch.empty(tuple(q.shape[:-2]) + (self.k,), dtype=torch.int32, device=dev)
         probe = pks.make_args(k=self.k, topk_idx=self.topk_idx, out=self.out,
-                              attn_splits=attn_splits, topk_mode=topk_mode, **t)
+                              attn_splits=attn_splits, topk_mode=topk_mode,
+                              wait_limit=wait_limit, **t)
         nbytes = pks.pks_decode_workspace_size(probe)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         if self.workspace.data_ptr() % 256:
             raise RuntimeError("workspace allocation is not 256-byte aligned")
         self.args = pks.make_args(k=self.k, topk_idx=self.topk_idx, out=self.out,
                                   workspace=self.workspace, attn_splits=attn_splits,
-                                  topk_mode=topk_mode, **t)
+                                  topk_mode=topk_mode, wait_limit=wait_limit, **t)
         pks.pks_decode_workspace_init(self.args, stream)
 
     def __call__(self, stream=None):
@@ -110,7 +111,7 @@ class MlaAttention:
     (bf16), topk_idx [B, k] (int32), d = 512 latent values."""
 
     def __init__(self, seq_lens, block_table, topk_idx, q, kv, sm_scale: float = 0.0,
-                 trim: bool = False, splits: int = 0, stream=None):
+                 trim: bool = False, splits: int = 0, stream=None, wait_limit: int = 0):
         dev = q.device
         self.out = torch.empty((q.shape[0], q.shape[1], 512), dtype=torch.bfloat16, device=dev)
         probe = pks.make_mla_args(seq_lens=seq_lens, block_table=block_table, topk_idx=topk_idx,
@@ -121,7 +122,7 @@ class MlaAttention:
         self.args = pks.make_mla_args(seq_lens=seq_lens, block_table=block_table,
                                       topk_idx=topk_idx, q=q, kv=kv, out=self.out,
                                       workspace=self.workspace, sm_scale=sm_scale, trim=trim,
-                                      splits=splits)
+                                      splits=splits, wait_limit=wait_limit)
         self._keep = (seq_lens, block_table, topk_idx, q, kv)
 
     def __call__(self, stream=None):

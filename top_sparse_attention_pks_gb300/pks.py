@@ -49,7 +49,7 @@ class pks_decode_args(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("attn_splits", ctypes.c_int32), ("topk_mode", ctypes.c_int32),
         ("n_queries", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1),
-        ("w_idx_f", ctypes.c_void_p), ("idx_fp8", ctypes.c_int32), ("reserved2", ctypes.c_int32),
+        ("w_idx_f", ctypes.c_void_p), ("idx_fp8", ctypes.c_int32), ("wait_limit", ctypes.c_int32),
     ]
 
 
@@ -62,7 +62,7 @@ class pks_mla_args(ctypes.Structure):
         ("topk_idx", ctypes.c_void_p), ("q", ctypes.c_void_p), ("kv", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t), ("sm_scale", ctypes.c_float),
-        ("trim", ctypes.c_int32), ("splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1),
+        ("trim", ctypes.c_int32), ("splits", ctypes.c_int32), ("wait_limit", ctypes.c_int32),
     ]
 
 
@@ -134,6 +134,8 @@ def _declare(L):
     L.pks_indexer_scores.restype = _ST
     L.pks_sparse_attention.argtypes = [_PARGS, _P]
     L.pks_sparse_attention.restype = _ST
+    L.pks_decode_barrier_offset.argtypes = [_PARGS, ctypes.POINTER(ctypes.c_size_t)]
+    L.pks_decode_barrier_offset.restype = _ST
     L.pks_decode_device_error.argtypes = [_PARGS, _P, _P]
     L.pks_decode_device_error.restype = _ST
     L.pks_residency_state_bytes.argtypes = [_I32, _I32, ctypes.POINTER(ctypes.c_size_t)]
@@ -286,7 +288,7 @@ class Pool:
 def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: int,
               topk_idx=None, out=None, workspace=None, attn_splits: int = 0,
               topk_mode: int = 0, num_pages: Optional[int] = None,
-              w_idx_f=None, idx_fp8: bool = False) -> pks_decode_args:
+              w_idx_f=None, idx_fp8: bool = False, wait_limit: int = 0) -> pks_decode_args:
     """Fill a ``pks_decode_args`` from tensors (shapes are read off the tensors).
 
     ``q`` is [B, Hq, D], or [B, Nq, Hq, D] for Nq query tokens per request (then
@@ -332,6 +334,7 @@ def make_args(*, seq_lens, block_table, q, q_idx, w_idx, kv_k, kv_v, idx_k, k: i
     a.topk_mode = int(topk_mode)
     a.w_idx_f = _dptr(w_idx_f, torch.float32, "w_idx_f")
     a.idx_fp8 = 1 if idx_fp8 else 0
+    a.wait_limit = int(wait_limit)
     return a
 
 
@@ -441,6 +444,14 @@ def pks_sparse_attention_static(args: pks_decode_args, stream=None) -> None:
            "pks_sparse_attention_static")
 
 
+def pks_decode_barrier_offset(args: pks_decode_args) -> int:
+    """Byte offset of the top-k request barriers' arrival counters in the workspace."""
+    n = ctypes.c_size_t()
+    _check(lib().pks_decode_barrier_offset(ctypes.byref(args), ctypes.byref(n)),
+           "pks_decode_barrier_offset")
+    return n.value
+
+
 def pks_decode_device_error(args: pks_decode_args, stream=None) -> int:
     code = ctypes.c_int32()
     _check(lib().pks_decode_device_error(ctypes.byref(args), ctypes.addressof(code),
@@ -530,7 +541,8 @@ class ResidencyTable:
 
 def make_mla_args(*, seq_lens, block_table, topk_idx, q, kv, out=None, workspace=None,
                   sm_scale: float = 0.0, trim: bool = False, splits: int = 0,
-                  d_latent: int = 512, num_pages: Optional[int] = None) -> pks_mla_args:
+                  d_latent: int = 512, num_pages: Optional[int] = None,
+                  wait_limit: int = 0) -> pks_mla_args:
     """Fill a ``pks_mla_args``: q [B, H, d + r], kv [num_pages, page_size, d + r],
     topk_idx [B, k], out [B, H, d] (bf16 / int32 tensors on the device)."""
     a = pks_mla_args()
@@ -554,6 +566,7 @@ def make_mla_args(*, seq_lens, block_table, topk_idx, q, kv, out=None, workspace
     a.sm_scale = float(sm_scale)
     a.trim = 1 if trim else 0
     a.splits = int(splits)
+    a.wait_limit = int(wait_limit)
     return a
 
 
