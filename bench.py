@@ -35,7 +35,8 @@ sys.path.insert(0, str(ROOT))
 from top_sparse_attention_pks_gb300 import build as pkg_build  # noqa: E402
 from top_sparse_attention_pks_gb300 import pks  # noqa: E402
 from top_sparse_attention_pks_gb300.decoder import MlaDecodeStep, SparseDecodeStep  # noqa: E402
-from top_sparse_attention_pks_gb300.workloads import (MLA_LATENT, MLA_WORKLOADS,  # noqa: E402
+from top_sparse_attention_pks_gb300.workloads import (HISPARSE_WORKLOADS,  # noqa: E402
+                                                      MLA_LATENT, MLA_WORKLOADS,
                                                       WORKLOADS, draw_float_weights,
                                                       draw_fp8_indexer, draw_host,
                                                       draw_mla_tensors, draw_tensors)
@@ -62,6 +63,17 @@ class L2Flush:
         self.r.sum()
 
 
+def repo_libraries():
+    """Shared objects of this repository mapped into this process."""
+    try:
+        maps = Path("/proc/self/maps").read_text().splitlines()
+    except OSError:
+        return []
+    root = str(ROOT)
+    return sorted({Path(ln.split()[-1]).name for ln in maps
+                   if ln.split()[-1].startswith(root) and ln.split()[-1].endswith(".so")})
+
+
 def measured_peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -72,11 +84,25 @@ def measured_peaks():
 
 # ------------------------------------------------------------------ setup --
 
-def setup(wl, device, seed_offset=0):
-    h = draw_host(wl)
+def block_table(wl, h, reference=False):
+    """The batch's block table: from the library's page pool, or, for the
+    oracle's arm (which loads nothing of the library), from the oracle's own
+    allocator (the two are checked equal by the host tests)."""
+    if reference:
+        import oracle
+        bt, _ = oracle.build_block_table(h["seq_lens"], wl.page_size, wl.max_pages,
+                                         wl.num_pages, h["prefix_group"], wl.prefix_len,
+                                         h["free_order"])
+        return bt
     pool = pks.Pool(wl.num_pages, wl.page_size, h["free_order"])
     bt, _ = pool.build_block_table(h["seq_lens"], wl.max_pages, h["prefix_group"], wl.prefix_len)
     pool.close()
+    return bt
+
+
+def setup(wl, device, seed_offset=0, reference=False):
+    h = draw_host(wl)
+    bt = block_table(wl, h, reference)
     t = draw_tensors(wl, device, seed_offset)
     t["seq_lens"] = h["seq_lens"].to(device)
     t["block_table"] = torch.from_numpy(bt).to(device)
@@ -256,7 +282,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="b16_128k",
-                    choices=sorted(WORKLOADS) + sorted(MLA_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(MLA_WORKLOADS) + sorted(HISPARSE_WORKLOADS))
     ap.add_argument("--impl", default="pks", choices=["pks", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-steps", type=int, default=200)
@@ -266,6 +292,8 @@ def main():
     ap.add_argument("--topk", type=int, default=0, help="override the workload's k")
     ap.add_argument("--queries", type=int, default=1,
                     help="query tokens per request (each scores, selects and attends alone)")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="with --hisparse: layers, each with its own pools and table")
     ap.add_argument("--hisparse", action="store_true",
                     help="workloads with a slot table: K/V in pinned host memory, HBM slots, "
                          "misses fetched every step (select, update, fetch, attention)")
@@ -303,7 +331,11 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if rank == 0:
-        pkg_build.build_library()
+        if args.impl == "reference":
+            import oracle  # the reference arm runs the oracle alone: libpks is not built
+            oracle.build()
+        else:
+            pkg_build.build_library()
     if dist:
         dist.barrier()
     if args.mla:
@@ -311,12 +343,14 @@ def main():
         if dist:
             dist.destroy_process_group()
         return
-    wl = WORKLOADS[args.workload]
+    if (args.workload in HISPARSE_WORKLOADS) and not args.hisparse:
+        ap.error("HBM-residency workloads run with --hisparse")
+    wl = {**WORKLOADS, **HISPARSE_WORKLOADS}[args.workload]
     if args.requests:
         wl = shrink(wl, args.requests)
     if args.topk:
         wl = wl.replace(k=args.topk)
-    t, h, bt = setup(wl, dev, seed_offset=rank)
+    t, h, bt = setup(wl, dev, seed_offset=rank, reference=args.impl == "reference")
     if args.queries > 1:
         # Nq query tokens per request: seeded queries of shape [B, Nq, ...]
         gen = torch.Generator(device=dev)
@@ -343,7 +377,8 @@ def main():
                 "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores", "kind",
                                                      "sample")},
                 "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
+                        "d2h_bytes_per_step": 0},
+                "loaded_libraries": repo_libraries()}
         print(json.dumps(line), flush=True)
         if dist:
             dist.destroy_process_group()
@@ -521,11 +556,9 @@ def main():
         dist.destroy_process_group()
 
 
-def mla_setup(wl, device, seed_offset=0):
+def mla_setup(wl, device, seed_offset=0, reference=False):
     h = draw_host(wl)
-    pool = pks.Pool(wl.num_pages, wl.page_size, h["free_order"])
-    bt, _ = pool.build_block_table(h["seq_lens"], wl.max_pages, h["prefix_group"], wl.prefix_len)
-    pool.close()
+    bt = block_table(wl, h, reference)
     t = draw_mla_tensors(wl, device, seed_offset)
     t["seq_lens"] = h["seq_lens"].to(device)
     t["block_table"] = torch.from_numpy(bt).to(device)
@@ -621,7 +654,7 @@ def mla_bench(wl, args, dev, rank, world, dist):
         wl = shrink(wl, args.requests)
     if args.topk:
         wl = wl.replace(k=args.topk)
-    t, h, bt = mla_setup(wl, dev, seed_offset=rank)
+    t, h, bt = mla_setup(wl, dev, seed_offset=rank, reference=args.impl == "reference")
     if args.fp8_indexer:  # DSA's indexer: FP8 e4m3 queries and keys, real head weights
         args.float_weights = True
         t["q_idx"], t["idx_k"] = draw_fp8_indexer(wl, dev, seed_offset=rank)
@@ -642,7 +675,8 @@ def mla_bench(wl, args, dev, rank, world, dist):
                           "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores",
                                                                "kind", "sample")},
                           "e2e": {"value": ref["value"], "unit": UNIT,
-                                  "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                                  "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                          "loaded_libraries": repo_libraries()}),
               flush=True)
         return
     step = MlaDecodeStep(t, wl.k)
@@ -796,60 +830,89 @@ def mla_bench(wl, args, dev, rank, world, dist):
 
 def hisparse_bench(wl, t, h, args, dev, rank):
     """The decode step with the KV cache in pinned host memory and an LRU cache
-    of its pages in HBM: select, residency update, miss fetch, attention
-    through the table.  Prints one JSON line (rank 0)."""
-    from top_sparse_attention_pks_gb300.decoder import ResidentDecodeStep
-    host_k = t["kv_k"].cpu().pin_memory()
-    host_v = t["kv_v"].cpu().pin_memory()
-    t = dict(t)
-    del t["kv_k"], t["kv_v"]  # the pools now live in host memory only
+    of its pages in HBM, over ``--layers`` layers (each its own pools, table and
+    queries): select, residency update, miss fetch, attention through the
+    table.  Timed twice on separate tables: every call of every layer one after
+    another, and with each layer's fetch on a side stream under the
+    neighbouring layers' selection and attention.  Prints one JSON line."""
+    from top_sparse_attention_pks_gb300.decoder import ResidentLayers
+    n_layers = max(1, args.layers)
+    layers, q_var = [], []
+    for l in range(n_layers):
+        tl = dict(t) if l == 0 else setup(wl, dev, seed_offset=rank * 100 + l)[0]
+        hk = tl["kv_k"].cpu().pin_memory()
+        hv = tl["kv_v"].cpu().pin_memory()
+        tl = dict(tl)
+        del tl["kv_k"], tl["kv_v"]  # the pools live in host memory only
+        layers.append(dict(tensors=tl, host_k=hk, host_v=hv,
+                           init_pages=h["initial_resident"].numpy()))
+        # a decode step brings a new indexer query: 8 seeded ones in rotation
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1000 + 100 * rank + l)
+        q_var.append([torch.randint(-127, 128, tl["q_idx"].shape, dtype=torch.int8, device=dev,
+                                    generator=gen) for _ in range(8)])
     torch.cuda.empty_cache()
-    rs = ResidentDecodeStep(t, host_k, host_v, wl.k, wl.capacity,
-                            h["initial_resident"].numpy())
+    runs = {"serial": ResidentLayers(layers, wl.k, wl.capacity),
+            "overlapped": ResidentLayers(layers, wl.k, wl.capacity)}
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
     flush = L2Flush(dev)
-    page_bytes = host_k[0].numel() * host_k.element_size()
-    # a decode step brings a new indexer query: cycle through 8 seeded ones
-    # (copied into place before each step, outside the timed interval)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1000 + rank)
-    q_var = [torch.randint(-127, 128, t["q_idx"].shape, dtype=torch.int8, device=dev,
-                           generator=gen) for _ in range(8)]
-    with torch.cuda.stream(s):
-        for i in range(args.warmup):
-            t["q_idx"].copy_(q_var[i % 8])
-            rs(s)
-    torch.cuda.synchronize()
-    n = max(1, min(args.steps, 200))
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
-    fetched = []
-    for i in range(n):
+    page_bytes = layers[0]["host_k"][0].numel() * layers[0]["host_k"].element_size()
+
+    def set_queries(i):
+        for l, L in enumerate(layers):
+            L["tensors"]["q_idx"].copy_(q_var[l][i % 8])
+
+    n = max(1, min(args.steps, 100))
+    res = {}
+    for name, run in runs.items():
         with torch.cuda.stream(s):
-            t["q_idx"].copy_(q_var[(args.warmup + i) % 8])
+            for i in range(args.warmup):
+                set_queries(i)
+                run(s, overlap=name == "overlapped")
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        fetched = []
+        for i in range(n):
+            with torch.cuda.stream(s):
+                set_queries(args.warmup + i)
+                flush()
+                ev[i][0].record(s)
+                run(s, overlap=name == "overlapped")
+                ev[i][1].record(s)
+            if i < 10:  # admitted misses of this step, all layers
+                torch.cuda.synchronize()
+                k = 0
+                for lay in run.layers:
+                    nm = int(lay.n_miss.item())
+                    ps = lay.table.page_slot()[lay.miss[:nm].long()]
+                    k += int((ps >= 0).sum().item())
+                fetched.append(k)
+        torch.cuda.synchronize()
+        res[name] = (float(np.median([e[0].elapsed_time(e[1]) for e in ev])),
+                     float(np.mean(fetched)))
+    # the four calls of layer 0, one after another, timed alone
+    lay = runs["serial"].layers[0]
+    st = []
+    for i in range(min(n, 20)):
+        with torch.cuda.stream(s):
+            set_queries(i)
             flush()
-            e = ev[i]
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             e[0].record(s)
-            pks.pks_decode_select(rs.args, s)
+            lay.select(s)
             e[1].record(s)
-            rs.table.update(rs.step.topk_idx, rs.block_table, rs.page_size, rs.miss, rs.n_miss, s)
+            lay.update(s)
             e[2].record(s)
-            rs.table.fetch(rs.miss, rs.n_miss, rs.host_k, rs.host_v, rs.slot_k, rs.slot_v, s)
+            lay.fetch(s)
             e[3].record(s)
-            pks.pks_sparse_attention_resident(rs.args, rs.table.state, rs.capacity, rs.slot_k,
-                                              rs.slot_v, s)
+            lay.attend(s)
             e[4].record(s)
-        if i < 20:  # admitted misses of this step (slots that now hold a missed page)
-            torch.cuda.synchronize()
-            nm = int(rs.n_miss.item())
-            ps = rs.table.page_slot()[rs.miss[:nm].long()]
-            fetched.append(int((ps >= 0).sum().item()))
-    torch.cuda.synchronize()
-    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])
-    med = np.median(stage, axis=0)
-    step_ms = float(np.median(stage.sum(axis=1)))
-    fetch_pages = float(np.mean(fetched))
-    fetch_bytes = 2 * fetch_pages * page_bytes
+        torch.cuda.synchronize()
+        st.append([e[j].elapsed_time(e[j + 1]) for j in range(4)])
+    med = np.median(np.array(st), axis=0)
+    step_ms, fetch_pages = res["overlapped"]
+    fetch_bytes = 2 * fetch_pages * page_bytes / n_layers
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": 1e3 / step_ms, "unit": UNIT, "n_gpus": 1,
@@ -857,13 +920,16 @@ def hisparse_bench(wl, t, h, args, dev, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": dict(config_dict(wl, args), kv_pools="pinned host memory",
-                           hbm_slots=wl.capacity),
-            "stages_ms": {"select": med[0], "residency_update": med[1], "fetch": med[2],
-                          "attention": med[3]},
-            "fetch": {"pages_per_step": fetch_pages, "bytes_per_step": fetch_bytes,
-                      "gbs": fetch_bytes / (med[2] * 1e-3) / 1e9},
-            "timing": "CUDA events between the four calls, L2 flushed (256 MB write + 256 MB read) before each step",
-            "queries": "a new seeded indexer query each step (8 in rotation)",
+                           hbm_slots=wl.capacity, layers=n_layers),
+            "step_ms": {"overlapped": step_ms, "serial": res["serial"][0]},
+            "layer0_stages_ms": {"select": med[0], "residency_update": med[1],
+                                 "fetch": med[2], "attention": med[3]},
+            "fetch": {"pages_per_layer_step": fetch_pages / n_layers,
+                      "bytes_per_layer_step": fetch_bytes,
+                      "gbs_alone": fetch_bytes / (med[2] * 1e-3) / 1e9 if med[2] > 0 else None},
+            "timing": "CUDA events around each step (all layers), L2 flushed (256 MB write + "
+                      "256 MB read) before each step; median over the steps",
+            "queries": "a new seeded indexer query each step (8 in rotation per layer)",
         }), flush=True)
 
 

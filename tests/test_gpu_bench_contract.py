@@ -44,9 +44,13 @@ def test_bench_line(extra):
     assert d["config"]["workload"]
 
 
-def test_reference_arm_line():
-    d = _run("--impl", "reference", "--steps", "3", "--warmup", "3")
+@pytest.mark.parametrize("extra", [[], ["--mla"]])
+def test_reference_arm_line(extra):
+    d = _run("--impl", "reference", "--steps", "3", "--warmup", "3", *extra)
     assert d["impl"] == "reference"
+    # the oracle alone: the library's shared object is never loaded on this arm
+    assert "liboracle.so" in d["loaded_libraries"]
+    assert "libpks.so" not in d["loaded_libraries"]
     assert {"metric", "value", "unit", "ms_per_step", "cpu_baseline", "e2e"} <= d.keys()
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]

@@ -85,3 +85,52 @@ def test_b32_4k_reduced_through_the_table():
     wl = WORKLOADS["b32_4k"].replace(B=4, seq_lens=(4096, 3000, 4096, 100), num_pages=256)
     admitted, overflow = _run(wl, capacity=96, n_init=40, steps=3, seed=7)
     assert admitted > 0
+
+
+def test_layers_with_the_fetch_overlapped():
+    # three layers, each with its own pools, table and queries; the fetch of a
+    # layer runs on a side stream under the neighbouring layers' selection and
+    # attention.  Against the same layers run one call after another, the
+    # oracle's residency per layer, the attention on each pool wholly in HBM
+    # and the oracle's attention.
+    from top_sparse_attention_pks_gb300.decoder import ResidentLayers
+    wl = WORKLOADS["b32_4k"].replace(B=4, seq_lens=(4096, 3000, 4096, 100), num_pages=256)
+    capacity, n_layers = 96, 3
+    layers, refs, fulls, bts = [], [], [], []
+    for l in range(n_layers):
+        t, _, bt = prepare(wl, seed_offset=l)
+        init = np.random.default_rng(40 + l).choice(wl.num_pages, size=40, replace=False)
+        layers.append(dict(tensors=t, host_k=t["kv_k"].cpu().pin_memory(),
+                           host_v=t["kv_v"].cpu().pin_memory(), init_pages=init))
+        refs.append(oracle.Residency(wl.num_pages, capacity, init))
+        fulls.append(SparseDecodeStep(t, wl.k))
+        bts.append(bt)
+    over = ResidentLayers(layers, wl.k, capacity)
+    serial = ResidentLayers(layers, wl.k, capacity)
+    admitted = 0
+    for step in range(3):
+        for L in layers:
+            t = L["tensors"]
+            t["q"].copy_(torch.randn_like(t["q"].float()).to(torch.bfloat16))
+            t["q_idx"].copy_(torch.randint(-127, 128, t["q_idx"].shape, dtype=torch.int8,
+                                           device="cuda"))
+        got = over(overlap=True)
+        ser = serial(overlap=False)
+        torch.cuda.synchronize()
+        for l, L in enumerate(layers):
+            t = L["tensors"]
+            out, idx = got[l]
+            _, ref_idx = oracle_topk(wl, t)
+            assert (host(idx).numpy() == ref_idx).all(), f"step {step} layer {l}: top-k"
+            miss_ref, _ = refs[l].step(ref_idx, bts[l], wl.page_size)
+            lay = over.layers[l]
+            n = int(lay.n_miss.item())
+            assert n == len(miss_ref) and (host(lay.miss[:n]).numpy() == miss_ref).all()
+            admitted += int((refs[l].page_slot[miss_ref] >= 0).sum()) if n else 0
+            assert torch.equal(out, ser[l][0]), f"step {step} layer {l}: overlapped != serial"
+            fulls[l].topk_idx.copy_(idx)
+            fulls[l].attention_only()
+            torch.cuda.synchronize()
+            assert torch.equal(out, fulls[l].out), f"step {step} layer {l}: != pool in HBM"
+            check_attention(out, oracle_attention(wl, t, ref_idx), f"step {step} layer {l}")
+    assert admitted > 0

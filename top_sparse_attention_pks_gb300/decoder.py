@@ -94,15 +94,78 @@ class ResidentDecodeStep:
         self.miss = torch.empty(num_pages, dtype=torch.int32, device=dev)
         self.n_miss = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def __call__(self, stream=None):
+    # the step's four calls, in order
+    def select(self, stream=None):
         pks.pks_decode_select(self.args, stream)
+
+    def update(self, stream=None):
         self.table.update(self.step.topk_idx, self.block_table, self.page_size, self.miss,
                           self.n_miss, stream)
+
+    def fetch(self, stream=None):
         self.table.fetch(self.miss, self.n_miss, self.host_k, self.host_v, self.slot_k,
                          self.slot_v, stream)
+
+    def attend(self, stream=None):
         pks.pks_sparse_attention_resident(self.args, self.table.state, self.capacity, self.slot_k,
                                           self.slot_v, stream)
+
+    def __call__(self, stream=None):
+        self.select(stream)
+        self.update(stream)
+        self.fetch(stream)
+        self.attend(stream)
         return self.step.out, self.step.topk_idx
+
+
+class ResidentLayers:
+    """Several layers of the decode step through HBM residency tables, the
+    miss fetch overlapped layer by layer ("Sparse Attention on GLM5.3 and
+    HBM", HiSparse paragraph: the KV cache lives in host memory, an LRU cache
+    of it in HBM, misses of the top-k are loaded, the loads overlapped across
+    layers).  Every layer has its own KV pools in pinned host memory, its own
+    slot table and slot pools, and its own inputs (``tensors`` per layer).
+
+    With ``overlap`` the fetch of layer l runs on a side stream: it waits for
+    layer l's residency update (an event) and runs while the main stream
+    selects layer l+1 and attends layer l-1; layer l's attention waits for its
+    own fetch (a second event).  Without it the four calls of every layer run
+    one after the other on the main stream.  Both orders compute the same
+    values: each layer's fetch writes only that layer's slots, which only that
+    layer's attention reads."""
+
+    def __init__(self, layers: list, k: int, capacity: int, stream=None):
+        # layers: dicts with "tensors" (device inputs), "host_k", "host_v"
+        # (pinned [num_pages, P, Hkv, D]) and "init_pages"
+        self.layers = [ResidentDecodeStep(L["tensors"], L["host_k"], L["host_v"], k, capacity,
+                                          L["init_pages"], stream=stream) for L in layers]
+        dev = layers[0]["tensors"]["q"].device
+        self.side = torch.cuda.Stream(device=dev)
+        n = len(self.layers)
+        self.updated = [torch.cuda.Event() for _ in range(n)]
+        self.fetched = [torch.cuda.Event() for _ in range(n)]
+
+    def __call__(self, stream=None, overlap: bool = True):
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if not overlap:
+            for L in self.layers:
+                L(main)
+            return [(L.step.out, L.step.topk_idx) for L in self.layers]
+        side = self.side
+        n = len(self.layers)
+        for l in range(n + 1):
+            if l < n:
+                L = self.layers[l]
+                L.select(main)
+                L.update(main)
+                self.updated[l].record(main)
+                side.wait_event(self.updated[l])
+                L.fetch(side)
+                self.fetched[l].record(side)
+            if l > 0:  # the previous layer's attention, once its own fetch is done
+                main.wait_event(self.fetched[l - 1])
+                self.layers[l - 1].attend(main)
+        return [(L.step.out, L.step.topk_idx) for L in self.layers]
 
 
 class MlaAttention:

@@ -27,6 +27,10 @@ Their ``Hq`` is the MLA head count H, ``D`` the key width d + r, ``Hkv`` 1:
 * ``mla_b16_128k``       - 16 x 131072 tokens, H = 128, top-2048.
 * ``mla_b64_32k_h64``    - 64 x 32768 tokens, H = 64, top-2048.
 
+``hs_b16_32k`` (below) is the HBM-residency workload of the miss fetch
+(HiSparse paragraph): a top-k that leaves about a third of the pages
+unselected, and a slot table for three quarters of the pages.
+
 Value distributions: K/V and attention queries are N(0, 1) rounded to bf16
 (round to nearest even); indexer queries and keys are integers uniform in
 [-127, 127]; indexer head weights are all one ("summed").
@@ -119,6 +123,18 @@ MLA_WORKLOADS = {
         name="mla_b64_32k_h64", B=64, seq_lens=(32768,) * 64, page_size=64, Hq=64, Hkv=1,
         D=576, Hi=1, Di=128, k=2048, num_pages=32768, max_pages=512, seed=14,
         permute_pool=True),
+}
+
+
+#: HBM-residency workloads whose top-k leaves pages unselected, so that a
+#: slot table larger than one step's pages admits the misses of the next:
+#: 16 x 32768 tokens in 16-token pages, top-2048 (about 64% of a request's
+#: pages touched per step), 75% of the pages fit in HBM.
+HISPARSE_WORKLOADS = {
+    "hs_b16_32k": Workload(
+        name="hs_b16_32k", B=16, seq_lens=(32768,) * 16, page_size=16, Hq=64, Hkv=8, D=128,
+        Hi=4, Di=128, k=2048, num_pages=16 * 2048, max_pages=2048, seed=5,
+        capacity=24576, initial_resident=24576),
 }
 
 
