@@ -52,6 +52,7 @@ def test_paging_example_config(topk_mode):
     dict(permute_pool=True),
     dict(Hi=2), dict(Hi=4), dict(Hi=8), dict(Di=128), dict(D=128),
     dict(Hq=8, Hkv=8), dict(Hq=16, Hkv=1), dict(Hq=12, Hkv=4),
+    dict(Hq=128, Hkv=8, D=128), dict(Hq=40, Hkv=4),
     dict(seq_lens=(0, 1, 2, 63, 64)),
     dict(seq_lens=(512, 512, 1, 511, 500), num_pages=160),
 ])

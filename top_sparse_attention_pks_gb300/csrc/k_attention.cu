@@ -14,9 +14,13 @@
 // into a 3-stage shared-memory ring; rows are stored XOR-swizzled by 16-byte
 // chunk so that ldmatrix reads are free of bank conflicts.  Each warp owns one
 // KV head and keeps an online-softmax state for the G query heads that share
-// it: S = Q K^T and O += P V run on the tensor cores (bf16 in, fp32
-// accumulate) with the G heads as the 16-row M dimension, padded with zero
-// rows.  A CTA that owns a whole (group, request) segment writes its bf16
+// it.  Both products run transposed on the tensor cores (bf16 in, fp32
+// accumulate), with the G heads as the 8-wide N dimension of m16n8k16 (one
+// column tile for G <= 8, two for G <= 16): S^T = K Q^T takes the 16 tokens
+// of a tile as M, and O^T += V^T P^T the head dimension as M, so no MMA
+// carries padding rows and O^T needs D / 4 accumulators a thread per column
+// tile.  P^T moves from the accumulator layout of S^T to the B-operand layout
+// with one movmatrix transpose per 8x8 block.  A CTA that owns a whole (group, request) segment writes its bf16
 // output; otherwise it writes a partial (m, l, o) to a slot indexed by
 // (CTA + segment), and k_attention_merge combines the partials of each split
 // segment by log-sum-exp rescaling.
@@ -60,6 +64,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+
+// transpose of an 8x8 bf16 matrix held one pair a thread in the mma layout
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
 }
 
 // D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulators
@@ -122,7 +133,7 @@ __device__ __forceinline__ int owner_cta(int64_t f, int64_t T, int64_t G) {
 
 // RES: K/V through a residency table (slot pools plus the host pool); the
 // plain instantiation keeps the host-row select out of the copy loop.
-template <int D, int HG, bool RES>
+template <int D, int HG, bool RES, int NGT>
 __global__ void __launch_bounds__(HG * 32, 1)
 k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv_k,
@@ -134,8 +145,8 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
                    float scale_log2, ResidentKv rk, int nq) {
   constexpr int NT = HG * 32;
   constexpr int CH = D / 8;   // 16-byte chunks per head row
-  constexpr int KS = D / 16;  // k-steps of S = Q K^T
-  constexpr int ND = D / 8;   // 8-wide column tiles of O
+  constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
+  constexpr int MT = D / 16;  // 16-row tiles of O^T (head dimension)
   constexpr int TILE = kAttnTile;
   constexpr int STAGE_ELEMS = TILE * HG * D;  // one of K or V
   const float kNegInf = __int_as_float(0xff800000);
@@ -227,66 +238,86 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     return c;
   };
 
-  const int ra = lane >> 2, rb = ra + 8, cq = (lane & 3) * 2;
-  uint32_t qa[KS][4];
-  float o[ND][4];
-  float m_a, m_b, l_a, l_b;
+  // mma fragment coordinates: g8 = lane / 4 (row group), t4 = lane % 4;
+  // column tile nt covers query heads nt * 8 + 2 * t4 + {0, 1} of the group
+  const int g8 = lane >> 2, t4 = lane & 3;
+  uint32_t qb[NGT][KS][2];   // Q^T as the B operand (dims x heads)
+  float o[NGT][MT][4];       // O^T accumulators (dims x heads)
+  float m_h[NGT][2], l_h[NGT][2];  // running max (log2 units) and partial sum per head
   auto reset_state = [&]() {
 #pragma unroll
-    for (int i = 0; i < ND; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    m_a = m_b = kNegInf;
-    l_a = l_b = 0.f;
+    for (int nt = 0; nt < NGT; ++nt) {
+#pragma unroll
+      for (int i = 0; i < MT; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+      m_h[nt][0] = m_h[nt][1] = kNegInf;
+      l_h[nt][0] = l_h[nt][1] = 0.f;
+    }
   };
   auto load_q = [&](int g, int b) {
     const int head = g * HG + warp;  // this warp's KV head
-    const __nv_bfloat16* qb = q + ((int64_t)b * Hq + (int64_t)head * G) * D;
+    const __nv_bfloat16* qb0 = q + ((int64_t)b * Hq + (int64_t)head * G) * D;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int col = ks * 16 + cq;
-      qa[ks][0] = ra < G ? *reinterpret_cast<const uint32_t*>(qb + ra * D + col) : 0u;
-      qa[ks][1] = rb < G ? *reinterpret_cast<const uint32_t*>(qb + rb * D + col) : 0u;
-      qa[ks][2] = ra < G ? *reinterpret_cast<const uint32_t*>(qb + ra * D + col + 8) : 0u;
-      qa[ks][3] = rb < G ? *reinterpret_cast<const uint32_t*>(qb + rb * D + col + 8) : 0u;
+    for (int nt = 0; nt < NGT; ++nt) {
+      const int j = nt * 8 + g8;  // query head of the group (B column)
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const __nv_bfloat16* src = qb0 + (int64_t)j * D + ks * 16 + t4 * 2;
+        qb[nt][ks][0] = j < G ? *reinterpret_cast<const uint32_t*>(src) : 0u;
+        qb[nt][ks][1] = j < G ? *reinterpret_cast<const uint32_t*>(src + 8) : 0u;
+      }
     }
   };
 
   // write this CTA's share of segment (g, b): the whole output when it owns
   // the whole segment, else a partial (m, l, o) that k_attention_merge combines
   auto finish_segment = [&](int g, int b, int64_t seg_lo, int64_t seg_hi) {
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    float l_t[NGT][2];
+#pragma unroll
+    for (int nt = 0; nt < NGT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float l = l_h[nt][e];  // sum over the 16 token rows: lanes of equal t4
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        l_t[nt][e] = l;
+      }
     const int head = g * HG + warp;
     const int c_first = owner_cta(seg_lo, T, GRID), c_last = owner_cta(seg_hi - 1, T, GRID);
-    __nv_bfloat16* ob = out + ((int64_t)b * Hq + (int64_t)head * G) * D;
     if (c_first == c_last) {
-      const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+      __nv_bfloat16* ob = out + ((int64_t)b * Hq + (int64_t)head * G) * D;
 #pragma unroll
-      for (int nd = 0; nd < ND; ++nd) {
-        const int d = nd * 8 + cq;
-        if (ra < G)
-          *reinterpret_cast<__nv_bfloat162*>(ob + ra * D + d) =
-              __floats2bfloat162_rn(o[nd][0] * ia, o[nd][1] * ia);
-        if (rb < G)
-          *reinterpret_cast<__nv_bfloat162*>(ob + rb * D + d) =
-              __floats2bfloat162_rn(o[nd][2] * ib, o[nd][3] * ib);
-      }
+      for (int nt = 0; nt < NGT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = nt * 8 + 2 * t4 + e;
+          if (j >= G) continue;
+          const float il = l_t[nt][e] > 0.f ? 1.f / l_t[nt][e] : 0.f;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            ob[(int64_t)j * D + mt * 16 + g8] = __float2bfloat16(o[nt][mt][e] * il);
+            ob[(int64_t)j * D + mt * 16 + g8 + 8] = __float2bfloat16(o[nt][mt][e + 2] * il);
+          }
+        }
       return;
     }
     const int seg = g * B + b;
     const int64_t slot = (int64_t)cta + seg;
     const int64_t base = (slot * HG + warp) * G;
 #pragma unroll
-    for (int nd = 0; nd < ND; ++nd) {
-      const int d = nd * 8 + cq;
-      if (ra < G) *reinterpret_cast<float2*>(part_o + (base + ra) * D + d) = make_float2(o[nd][0], o[nd][1]);
-      if (rb < G) *reinterpret_cast<float2*>(part_o + (base + rb) * D + d) = make_float2(o[nd][2], o[nd][3]);
-    }
-    if ((lane & 3) == 0) {
-      if (ra < G) part_ml[base + ra] = make_float2(m_a, l_a);
-      if (rb < G) part_ml[base + rb] = make_float2(m_b, l_b);
-    }
+    for (int nt = 0; nt < NGT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = nt * 8 + 2 * t4 + e;
+        if (j >= G) continue;
+        float* po = part_o + (base + j) * D;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          po[mt * 16 + g8] = o[nt][mt][e];
+          po[mt * 16 + g8 + 8] = o[nt][mt][e + 2];
+        }
+        if (g8 == 0) part_ml[base + j] = make_float2(m_h[nt][e], l_t[nt][e]);
+      }
   };
 
   // consumer cursor: segment whose state the warps hold
@@ -397,65 +428,69 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
 
       const __nv_bfloat16* sk = s_kv + (size_t)(tile % kAttnStages) * 2 * STAGE_ELEMS;
       const __nv_bfloat16* sv = sk + STAGE_ELEMS;
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // S^T = K Q^T: 16 tokens (M) x 8 heads (N) per column tile, two
+      // accumulator chains (even and odd k-steps) for latency
+      float sacc[2][NGT][4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int nt = 0; nt < NGT; ++nt) sacc[c][nt][0] = sacc[c][nt][1] = sacc[c][nt][2] = sacc[c][nt][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const int row = ((lane >> 4) << 3) + (lane & 7);
-        const int chunk = 2 * ks + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(sk + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), b0, b1, b2, b3);
-        mma_bf16(sacc[0], qa[ks], b0, b1);
-        mma_bf16(sacc[1], qa[ks], b2, b3);
-      }
-      float x[2][4];
+        const int row = (lane & 7) + (((lane >> 3) & 1) << 3);  // token
+        const int chunk = 2 * ks + (lane >> 4);
+        uint32_t a[4];
+        ldsm_x4(smem_u32(sk + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), a[0], a[1], a[2], a[3]);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NGT; ++nt) mma_bf16(sacc[ks & 1][nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+      }
+      // rows g8 and g8 + 8 of the tile; masked tokens score -inf
+      const bool v0 = g8 < n && s_row[rbase + g8] != -1;
+      const bool v1 = g8 + 8 < n && s_row[rbase + g8 + 8] != -1;
+      uint32_t pb[NGT][2];  // P^T as the B operand (tokens x heads)
+#pragma unroll
+      for (int nt = 0; nt < NGT; ++nt) {
+        float x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float sv_ = sacc[0][nt][i] + sacc[1][nt][i];
+          x[i] = (i < 2 ? v0 : v1) ? sv_ * scale_log2 : kNegInf;
+        }
+        float al[2], p[4];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int r = nt * 8 + cq + e;
-          const bool valid = r < n && s_row[rbase + r] != -1;
-          x[nt][e] = valid ? sacc[nt][e] * scale_log2 : kNegInf;
-          x[nt][e + 2] = valid ? sacc[nt][e + 2] * scale_log2 : kNegInf;
+          // column max over the 16 tokens: own two rows, then lanes of equal t4
+          float mx = fmaxf(x[e], x[e + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mn = fmaxf(m_h[nt][e], mx);
+          al[e] = mn == kNegInf ? 1.f : exp2f(m_h[nt][e] - mn);
+          p[e] = x[e] == kNegInf ? 0.f : exp2f(x[e] - mn);
+          p[e + 2] = x[e + 2] == kNegInf ? 0.f : exp2f(x[e + 2] - mn);
+          l_h[nt][e] = l_h[nt][e] * al[e] + (p[e] + p[e + 2]);
+          m_h[nt][e] = mn;
         }
-      }
-      float mx_a = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-      float mx_b = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-      const float al_a = mn_a == kNegInf ? 1.f : exp2f(m_a - mn_a);
-      const float al_b = mn_b == kNegInf ? 1.f : exp2f(m_b - mn_b);
-      float p[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        p[nt][0] = x[nt][0] == kNegInf ? 0.f : exp2f(x[nt][0] - mn_a);
-        p[nt][1] = x[nt][1] == kNegInf ? 0.f : exp2f(x[nt][1] - mn_a);
-        p[nt][2] = x[nt][2] == kNegInf ? 0.f : exp2f(x[nt][2] - mn_b);
-        p[nt][3] = x[nt][3] == kNegInf ? 0.f : exp2f(x[nt][3] - mn_b);
+        for (int mt = 0; mt < MT; ++mt) {
+          o[nt][mt][0] *= al[0];
+          o[nt][mt][1] *= al[1];
+          o[nt][mt][2] *= al[0];
+          o[nt][mt][3] *= al[1];
+        }
+        // (token g8, heads 2 t4 + {0,1}) -> (tokens 2 t4 + {0,1}, head g8)
+        pb[nt][0] = movmatrix_t(pack_bf16(p[0], p[1]));
+        pb[nt][1] = movmatrix_t(pack_bf16(p[2], p[3]));
       }
-      l_a = l_a * al_a + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-      l_b = l_b * al_b + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-      m_a = mn_a;
-      m_b = mn_b;
+      // O^T += V^T P^T: 16 dims (M) x 8 heads (N), k = the 16 tokens
 #pragma unroll
-      for (int i = 0; i < ND; ++i) {
-        o[i][0] *= al_a;
-        o[i][1] *= al_a;
-        o[i][2] *= al_b;
-        o[i][3] *= al_b;
-      }
-      const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]),
-                              pack_bf16(p[1][0], p[1][1]), pack_bf16(p[1][2], p[1][3])};
+      for (int mt = 0; mt < MT; ++mt) {
+        const int row = (lane & 7) + ((lane >> 4) << 3);  // token
+        const int chunk = 2 * mt + ((lane >> 3) & 1);
+        uint32_t a[4];
+        ldsm_x4_t(smem_u32(sv + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), a[0], a[1], a[2], a[3]);
 #pragma unroll
-      for (int nd = 0; nd < ND; nd += 2) {
-        const int row = (((lane >> 3) & 1) << 3) + (lane & 7);
-        const int chunk = nd + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(sv + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), b0, b1, b2, b3);
-        mma_bf16(o[nd], pa, b0, b1);
-        mma_bf16(o[nd + 1], pa, b2, b3);
+        for (int nt = 0; nt < NGT; ++nt) mma_bf16(o[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
       __syncthreads();
       cs_pos += n;
@@ -576,7 +611,7 @@ size_t attn_smem_bytes(int B) {
 // batch cannot undo the limit that a larger one set.  Attribute calls are not
 // stream operations: after the first call at a size they stay out of any
 // graph capture.
-template <int D, int HG, bool RES>
+template <int D, int HG, bool RES, int NGT>
 cudaError_t attn_configure(size_t smem, int* blocks_per_sm) {
   static size_t configured[64] = {0};
   static int per_sm[64] = {0};
@@ -585,7 +620,7 @@ cudaError_t attn_configure(size_t smem, int* blocks_per_sm) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > configured[dev]) {
-    auto kern = k_sparse_attention<D, HG, RES>;
+    auto kern = k_sparse_attention<D, HG, RES, NGT>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int bps = 0;
@@ -598,16 +633,16 @@ cudaError_t attn_configure(size_t smem, int* blocks_per_sm) {
   return cudaSuccess;
 }
 
-template <int D, int HG, bool RES>
+template <int D, int HG, bool RES, int NGT>
 cudaError_t launch_attn_t(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
                           bool trim, const ResidentKv& rk, cudaStream_t s) {
-  auto kern = k_sparse_attention<D, HG, RES>;
+  auto kern = k_sparse_attention<D, HG, RES, NGT>;
   const int nq = query_count(a);
   const int Bv = a.B * nq;  // virtual requests
   const size_t smem = attn_smem_bytes<D, HG>(Bv);
   int bps = 1;
   {
-    cudaError_t e = attn_configure<D, HG, RES>(smem, &bps);
+    cudaError_t e = attn_configure<D, HG, RES, NGT>(smem, &bps);
     if (e != cudaSuccess) return e;
   }
   int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * bps;
@@ -664,15 +699,15 @@ StaticAttnLayout static_attn_layout(const pks_decode_args& a, int64_t grid) {
   return L;
 }
 
-template <int D, int HG>
+template <int D, int HG, int NGT>
 cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cudaStream_t s,
                                  bool* too_large) {
-  auto kern = k_sparse_attention<D, HG, false>;
+  auto kern = k_sparse_attention<D, HG, false, NGT>;
   const int nq = query_count(a);
   const int Bv = a.B * nq;
   const size_t smem = attn_smem_bytes<D, HG>(Bv);
   int bps = 1;
-  cudaError_t e = attn_configure<D, HG, false>(smem, &bps);
+  cudaError_t e = attn_configure<D, HG, false, NGT>(smem, &bps);
   if (e != cudaSuccess) return e;
   // the same grid pks_sparse_attention uses for these arguments
   int grid = a.attn_splits > 0 ? a.attn_splits : device_sm_count() * bps;
@@ -708,10 +743,15 @@ cudaError_t launch_attn_static_t(const pks_decode_args& a, uint8_t* scratch, cud
 cudaError_t launch_attention(const pks_decode_args& a, const WorkspaceLayout& L, uint8_t* ws,
                              bool trim, cudaStream_t s, const ResidentKv& rk) {
   const int hg = attn_heads_per_cta(a.Hkv);
-#define PKS_ATTN_CASE(D_, HG_) \
-  if (a.D == D_ && hg == HG_)                                                             \
-    return rk.page_slot ? launch_attn_t<D_, HG_, true>(a, L, ws, trim, rk, s)              \
-                        : launch_attn_t<D_, HG_, false>(a, L, ws, trim, rk, s);
+  const bool wide = a.Hq / a.Hkv > 8;  // two 8-head column tiles
+#define PKS_ATTN_CASE(D_, HG_)                                                             \
+  if (a.D == D_ && hg == HG_) {                                                            \
+    if (wide)                                                                              \
+      return rk.page_slot ? launch_attn_t<D_, HG_, true, 2>(a, L, ws, trim, rk, s)          \
+                          : launch_attn_t<D_, HG_, false, 2>(a, L, ws, trim, rk, s);        \
+    return rk.page_slot ? launch_attn_t<D_, HG_, true, 1>(a, L, ws, trim, rk, s)            \
+                        : launch_attn_t<D_, HG_, false, 1>(a, L, ws, trim, rk, s);          \
+  }
   PKS_ATTN_CASE(64, 1)
   PKS_ATTN_CASE(64, 2)
   PKS_ATTN_CASE(64, 4)
@@ -748,8 +788,11 @@ cudaError_t launch_attention_static(const pks_decode_args& a, uint8_t* scratch, 
                                     bool* too_large) {
   *too_large = false;
   const int hg = attn_heads_per_cta(a.Hkv);
-#define PKS_ATTN_STATIC_CASE(D_, HG_) \
-  if (a.D == D_ && hg == HG_) return launch_attn_static_t<D_, HG_>(a, scratch, s, too_large);
+  const bool wide = a.Hq / a.Hkv > 8;
+#define PKS_ATTN_STATIC_CASE(D_, HG_)                                                       \
+  if (a.D == D_ && hg == HG_)                                                              \
+    return wide ? launch_attn_static_t<D_, HG_, 2>(a, scratch, s, too_large)               \
+                : launch_attn_static_t<D_, HG_, 1>(a, scratch, s, too_large);
   PKS_ATTN_STATIC_CASE(64, 1)
   PKS_ATTN_STATIC_CASE(64, 2)
   PKS_ATTN_STATIC_CASE(64, 4)
