@@ -356,7 +356,10 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
         s_row[f - chunk_lo] = row;
       }
     };
-    const int64_t early_hi = lmin(chunk_hi, chunk_lo + (int64_t)(kAttnStages - 1) * TILE);
+    // the first pass takes one position a thread (at least the ring's first
+    // tiles): as many rows resolve in one dependent round trip as in fewer
+    const int64_t early_hi =
+        lmin(chunk_hi, chunk_lo + (int64_t)(NT > (kAttnStages - 1) * TILE ? NT : (kAttnStages - 1) * TILE));
     resolve_rows(chunk_lo, early_hi);
     __syncthreads();
 
