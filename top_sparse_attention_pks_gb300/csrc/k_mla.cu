@@ -84,6 +84,7 @@ constexpr int kMaxCtaTiles = kMlaMaxCtaTiles;
 
 static_assert(kDK % 64 == 0 && kDL % 64 == 0, "latent and key widths in 64-value blocks");
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
+static_assert(kRows * (kHalf + 4) * 4 <= 2 * kKStageBytes, "O staged in the K stages");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -229,6 +230,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
+}
+
+// barrier `id` among `n` threads that also ANDs a predicate over them
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -587,44 +600,51 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       tc_fence_before();
       mbar_arrive(&bar_p);
     }
-    // ---- O of this CTA's half: to the output, or to the partial slot
-    if (ok && waitw(&bar_o, (ntiles - 1) & 1)) {
+    // ---- O of this CTA's half: to the output, or to the partial slot.  A
+    // thread's row is 512 contiguous bytes, so the rows go through shared
+    // memory (the K stages: every gather and MMA has completed once the last
+    // O update has) and leave as whole rows, 512 bytes a warp instruction,
+    // instead of 32 rows' 16-byte pieces
+    const bool have_o = ok && waitw(&bar_o, (ntiles - 1) & 1);
+    float* stage = reinterpret_cast<float*>(smem_raw + (sK - smem_u32(smem_raw)));
+    constexpr int kStageRow = kHalf + 4;  // floats; 16 bytes of padding spread the banks
+    if (have_o) {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      // the output is normalised here; partials keep (m, l) apart
+      const float scale = splits == 1 ? (l_run > 0.f ? 1.f / l_run : 0.f) : 1.f;
 #pragma unroll 1
       for (int c = ch * 4; c < ch * 4 + 4; ++c) {
         float ov[32];
         tmem_ld32(tmem + lane_off + kTmemO + c * 32, ov);
-        if (h < H) {
-          if (splits == 1) {
-            __nv_bfloat16* ob = out + ((int64_t)b * H + h) * kDL + half * kHalf + c * 32;
+        float* dst = stage + h * kStageRow + c * 32;
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 w;
-              __nv_bfloat162 p0 = __floats2bfloat162_rn(ov[i] * inv, ov[i + 1] * inv);
-              __nv_bfloat162 p1 = __floats2bfloat162_rn(ov[i + 2] * inv, ov[i + 3] * inv);
-              __nv_bfloat162 p2 = __floats2bfloat162_rn(ov[i + 4] * inv, ov[i + 5] * inv);
-              __nv_bfloat162 p3 = __floats2bfloat162_rn(ov[i + 6] * inv, ov[i + 7] * inv);
-              w.x = *reinterpret_cast<uint32_t*>(&p0);
-              w.y = *reinterpret_cast<uint32_t*>(&p1);
-              w.z = *reinterpret_cast<uint32_t*>(&p2);
-              w.w = *reinterpret_cast<uint32_t*>(&p3);
-              *reinterpret_cast<uint4*>(ob + i) = w;
-            }
-          } else {
-            float* po = part_o + (slot * H + h) * kDL + half * kHalf + c * 32;
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(po + i) =
-                  make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
-          }
-        }
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(dst + i) =
+              make_float4(ov[i] * scale, ov[i + 1] * scale, ov[i + 2] * scale, ov[i + 3] * scale);
       }
       if (splits > 1 && half == 0 && ch == 0 && h < H)
         part_ml[slot * H + h] = make_float2(m_run, l_run);
-    } else {
-      ok = false;
     }
+    // the 256 softmax threads: every row staged, unless a warp gave up
+    if (bar_and(1, kCons, have_o)) {
+      constexpr int kQ = kHalf / 4;  // float4 columns of a row
+      for (int idx = tid; idx < H * kQ; idx += kCons) {
+        const int r = idx / kQ, q4 = idx % kQ;
+        const float4 v = *reinterpret_cast<const float4*>(stage + r * kStageRow + q4 * 4);
+        if (splits == 1) {
+          __nv_bfloat16* ob = out + ((int64_t)b * H + r) * kDL + half * kHalf + q4 * 4;
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(v.x, v.y);
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(v.z, v.w);
+          uint2 w;
+          w.x = *reinterpret_cast<uint32_t*>(&p0);
+          w.y = *reinterpret_cast<uint32_t*>(&p1);
+          *reinterpret_cast<uint2*>(ob) = w;
+        } else {
+          *reinterpret_cast<float4*>(part_o + (slot * H + r) * kDL + half * kHalf + q4 * 4) = v;
+        }
+      }
+    }
+    if (!have_o) ok = false;
     if (!ok && lane == 0) {
       flag_error(err, kErrTimeout);
       s_abort = 1;
