@@ -276,8 +276,9 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
                 int num_pages, int k, int trim, int splits, float scale_log2,
                 long long budget) {
   extern __shared__ uint8_t smem_raw[];
-  // bar_full[i]: stage i gathered (gather warps); bar_s: S ready;
-  // bar_p: P written (128 softmax threads); bar_o: O update done
+  // bar_full[i]: stage i gathered (one arrival a gather warp); bar_s: S ready;
+  // bar_p: P written (one arrival a softmax warp); bar_o: O update done;
+  // bar_mx / bar_ps: every softmax warp has posted its rows' half max / sum
   // bar_free[i]: the O update of the last tile in stage i is done (the stage
   // may be refilled)
   __shared__ __align__(8) uint64_t bar_full[2], bar_free[2], bar_s, bar_p, bar_o, bar_mx, bar_ps;
@@ -335,15 +336,16 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
 
   if (warp == 0) tmem_alloc(&s_tmem, kTmemCols);
   if (tid == kCons) {
-    mbar_init(&bar_full[0], kGather);
-    mbar_init(&bar_full[1], kGather);
+    // one arrival a warp (after the warp's own fences and a __syncwarp)
+    mbar_init(&bar_full[0], kGather / 32);
+    mbar_init(&bar_full[1], kGather / 32);
     mbar_init(&bar_free[0], 1);
     mbar_init(&bar_free[1], 1);
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_p, kCons);
+    mbar_init(&bar_p, kCons / 32);
     mbar_init(&bar_o, 1);
-    mbar_init(&bar_mx, kCons);
-    mbar_init(&bar_ps, kCons);
+    mbar_init(&bar_mx, kCons / 32);
+    mbar_init(&bar_ps, kCons / 32);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     s_abort = 0;
   }
@@ -545,7 +547,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       }
       // the row's max over both halves (both threads get the same value)
       s_mx[ch][h] = mh;
-      mbar_arrive(&bar_mx);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_mx);
       if (!waitw(&bar_mx, t & 1)) {
         ok = false;
         break;
@@ -566,7 +569,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       }
       // the row's sum, added in the same order by both threads
       s_ps[ch][h] = ph;
-      mbar_arrive(&bar_ps);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ps);
       if (!waitw(&bar_ps, t & 1)) {
         ok = false;
         break;
@@ -598,7 +602,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       }
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_p);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p);
     }
     // ---- O of this CTA's half: to the output, or to the partial slot.  A
     // thread's row is 512 contiguous bytes, so the rows go through shared
@@ -679,7 +684,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       // this thread's copies have landed: visible to the tensor core, counted
       cp_async_wait_all();
       fence_async_smem();
-      mbar_arrive(&bar_full[st]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_full[st]);
     }
     if (!ok && lane == 0) {
       flag_error(err, kErrTimeout);
