@@ -553,14 +553,17 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
   if (tid == 0)
     chunk_cnt[(int64_t)b * nchunks_max + c] = make_int2(packed_total >> 16, packed_total & 0xffff);
 
-  // ---- barrier of the request's CTAs
+  // ---- barrier of the request's CTAs (a request of one chunk is one CTA:
+  // its own writes are visible to it after __syncthreads)
   __syncthreads();
-  if (tid == 0) request_arrive(w.tick + b);
-  if (tid == 0) sm.flag = request_wait(w.tick + b, nch, spins);
-  __syncthreads();
-  if (!sm.flag) {
-    if (tid == 0) atomicCAS(w.err, 0, kErrTimeout);
-    return;
+  if (nch > 1) {
+    if (tid == 0) request_arrive(w.tick + b);
+    if (tid == 0) sm.flag = request_wait(w.tick + b, nch, spins);
+    __syncthreads();
+    if (!sm.flag) {
+      if (tid == 0) atomicCAS(w.err, 0, kErrTimeout);
+      return;
+    }
   }
   // every CTA of the request is resident: the attention grid may now take
   // SM slots without keeping a CTA of this grid from its barrier
@@ -696,10 +699,12 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
       t.key = kstar;
       w.thr[b] = t;
     }
-    __threadfence();
-    if (atomicAdd(w.depart + b, 1) == nch - 1) {
-      w.tick[b] = 0;
-      w.depart[b] = 0;
+    if (nch > 1) {
+      __threadfence();
+      if (atomicAdd(w.depart + b, 1) == nch - 1) {
+        w.tick[b] = 0;
+        w.depart[b] = 0;
+      }
     }
   }
 }
