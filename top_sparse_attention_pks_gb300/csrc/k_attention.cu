@@ -20,14 +20,18 @@
 // of a tile as M, and O^T += V^T P^T the head dimension as M, so no MMA
 // carries padding rows and O^T needs D / 4 accumulators a thread per column
 // tile.  P^T moves from the accumulator layout of S^T to the B-operand layout
-// with one movmatrix transpose per 8x8 block.  A CTA that owns a whole (group, request) segment writes its bf16
-// output; otherwise it writes a partial (m, l, o) to a slot indexed by
-// (CTA + segment), and k_attention_merge combines the partials of each split
-// segment by log-sum-exp rescaling.
+// with one movmatrix transpose per 8x8 block.  A CTA that owns a whole
+// (group, request) segment writes its bf16 output; otherwise it writes a
+// partial (m, l, o) to a slot indexed by (CTA + segment), and
+// k_attention_merge combines the partials of each split segment by
+// log-sum-exp rescaling.
 //
 // At G = 8 query heads per KV head the work is about 8 FLOP per byte of K/V,
-// far below the tensor-core ridge: the kernel is bound by HBM bandwidth, and
-// the MMAs only keep the arithmetic off the critical path.
+// far below the tensor-core ridge: the MMAs only keep the arithmetic off the
+// critical path.  What bounds the kernel is the rate at which an SM streams
+// gathered rows through the ring (a 64 KB tile about every 1.5 us, 6.3 TB/s
+// over 152 SMs, measured), so the compute between a tile's arrival and its
+// release is kept short.
 
 #include <cuda_bf16.h>
 
@@ -358,8 +362,8 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
     };
     // the first pass takes one position a thread (at least the ring's first
     // tiles): as many rows resolve in one dependent round trip as in fewer
-    const int64_t early_hi =
-        lmin(chunk_hi, chunk_lo + (int64_t)(NT > (kAttnStages - 1) * TILE ? NT : (kAttnStages - 1) * TILE));
+    constexpr int kFirstPass = NT > (kAttnStages - 1) * TILE ? NT : (kAttnStages - 1) * TILE;
+    const int64_t early_hi = lmin(chunk_hi, chunk_lo + kFirstPass);
     resolve_rows(chunk_lo, early_hi);
     __syncthreads();
 
@@ -437,15 +441,19 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int nt = 0; nt < NGT; ++nt) sacc[c][nt][0] = sacc[c][nt][1] = sacc[c][nt][2] = sacc[c][nt][3] = 0.f;
+        for (int nt = 0; nt < NGT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sacc[c][nt][i] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int row = (lane & 7) + (((lane >> 3) & 1) << 3);  // token
         const int chunk = 2 * ks + (lane >> 4);
         uint32_t a[4];
-        ldsm_x4(smem_u32(sk + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), a[0], a[1], a[2], a[3]);
+        ldsm_x4(smem_u32(sk + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), a[0], a[1],
+                a[2], a[3]);
 #pragma unroll
-        for (int nt = 0; nt < NGT; ++nt) mma_bf16(sacc[ks & 1][nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+        for (int nt = 0; nt < NGT; ++nt)
+          mma_bf16(sacc[ks & 1][nt], a, qb[nt][ks][0], qb[nt][ks][1]);
       }
       // rows g8 and g8 + 8 of the tile; masked tokens score -inf
       const bool v0 = g8 < n && s_row[rbase + g8] != -1;
@@ -491,7 +499,8 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
         const int row = (lane & 7) + ((lane >> 4) << 3);  // token
         const int chunk = 2 * mt + ((lane >> 3) & 1);
         uint32_t a[4];
-        ldsm_x4_t(smem_u32(sv + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), a[0], a[1], a[2], a[3]);
+        ldsm_x4_t(smem_u32(sv + (row * HG + warp) * D + ((chunk ^ (row & 7)) << 3)), a[0], a[1],
+                  a[2], a[3]);
 #pragma unroll
         for (int nt = 0; nt < NGT; ++nt) mma_bf16(o[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
