@@ -13,13 +13,15 @@
 // value width), 512 threads: warps 0-7 are the softmax threads, two per row of
 // the MMA (query heads, zero rows above H; row h is tensor-memory lane h, read
 // by warps h / 32 and h / 32 + 4, each for half of the row's columns); warp 8
-// is the producer (MMA issue); warps 9-15 gather the K/V rows.
+// is the producer (MMA issue); warps 9-14 gather the K/V rows; warp 15 issues
+// the second half of S.
 // Per 64-token tile:
 //   S[128 x 64]   = Q[128 x 576] . K^T          tcgen05.mma, fp32 in TMEM
 //   P             = exp2(S * scale - m)         two threads per head row
 //   O[128 x 256] += P[128 x 64] . V[64 x 256]   tcgen05.mma, fp32 in TMEM
 // A tcgen05.mma costs about the same time for N = 32 or 64 and M = 64 or
-// 128 (measured), so S is computed 64 tokens at a time.  Tensor memory holds
+// 128 (measured): the cost is the issue, so S is computed 64 tokens at a
+// time, as two N = 32 halves issued side by side by two threads.  Tensor memory holds
 // O (256 columns: this CTA's half of the value width; all of O would fill
 // it, hence the two halves, which both compute S), S (64 columns) and Q's
 // values 0..383 (192 columns, the A operand of 24 of the 36 k-steps of S);
@@ -37,11 +39,14 @@
 //   gather warps: tile t into stage t & 1 once the O update of tile t - 2 has
 //     released the stage (bar_free), then publish it (bar_full);
 //   producer warp: issues O += P.V of tile t - 1 once its P is written (bar_p,
-//     commit -> bar_o and bar_free) and then S = Q.K^T of tile t once its
-//     gathers landed (bar_full, commit -> bar_s);
-//   softmax warps: after the O update of tile t - 1 (bar_o) take S of tile t
-//     (bar_s), exchange each row's max and sum between its two threads
-//     (bar_mx, bar_ps), rescale O if the max moved, write P (bar_p).
+//     commit -> bar_o and bar_free) and then S = Q.K^T of tile t's tokens
+//     0..31 once its gathers have landed (bar_full, commit -> bar_s[0]);
+//   issuer warp: S of tile t's tokens 32..63 on the same conditions
+//     (commit -> bar_s[1]);
+//   softmax warps: after the O update of tile t - 1 (bar_o) take their half
+//     of S of tile t (bar_s[half]), exchange each row's max and sum between
+//     its two threads (bar_mx, bar_ps), rescale O if the max moved, write P
+//     (bar_p).
 // So the tensor pipe runs O(t - 1) before S(t), and the next tile's gathers
 // run beside the softmax instead of in front of it.  With several splits per
 // request the CTAs write (m, l, O) partials that k_mla_merge combines.
@@ -62,8 +67,9 @@ constexpr int kRows = 128;                  // MMA M: query heads, zero padded
 constexpr int kHalf = kDL / 2;              // value columns per CTA
 constexpr int kCons = 2 * kRows;            // softmax threads: two per head row
 constexpr int kProdWarp = kCons / 32;       // warp 8: the producer
-constexpr int kGather = 224;                 // gather threads: warps 9-15 (512 threads a CTA)
-constexpr int kThreads = kCons + 32 + kGather;  // softmax, producer, gather warps
+constexpr int kGather = 192;                 // gather threads: warps 9-14
+constexpr int kIssueWarp = kProdWarp + 1 + kGather / 32;  // warp 15: issues S for tokens 32..63
+constexpr int kThreads = kCons + 32 + kGather + 32;  // 512: softmax, producer, gather, issuer
 constexpr int kBlk = kDK / 64;              // 64-value (128-byte) column blocks
 constexpr int kQTmemDims = 384;             // Q values 0..383 live in tensor memory
 constexpr int kQSmemBlk = (kDK - kQTmemDims) / 64;  // the rest: 3 column blocks in smem
@@ -264,7 +270,7 @@ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t kIdescS = idesc_bf16(kRows, kTile, false);   // S = Q . K^T
+constexpr uint32_t kIdescS = idesc_bf16(kRows, kTile / 2, false);  // S = Q . K^T, half the tokens
 constexpr uint32_t kIdescO = idesc_bf16(kRows, kHalf, true);    // O += P . V
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -276,12 +282,13 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
                 int num_pages, int k, int trim, int splits, float scale_log2,
                 long long budget) {
   extern __shared__ uint8_t smem_raw[];
-  // bar_full[i]: stage i gathered (one arrival a gather warp); bar_s: S ready;
+  // bar_full[i]: stage i gathered (one arrival a gather warp); bar_s[h]: S of
+  // the tile's tokens 32h .. 32h + 31 ready (two issuing threads);
   // bar_p: P written (one arrival a softmax warp); bar_o: O update done;
   // bar_mx / bar_ps: every softmax warp has posted its rows' half max / sum
   // bar_free[i]: the O update of the last tile in stage i is done (the stage
   // may be refilled)
-  __shared__ __align__(8) uint64_t bar_full[2], bar_free[2], bar_s, bar_p, bar_o, bar_mx, bar_ps;
+  __shared__ __align__(8) uint64_t bar_full[2], bar_free[2], bar_s[2], bar_p, bar_o, bar_mx, bar_ps;
   __shared__ uint32_t s_tmem;
   __shared__ int32_t s_row[kMaxCtaTiles][kTile];         // physical row of each position
   __shared__ uint32_t s_mask[kMaxCtaTiles][kTile / 32];  // positions with a row
@@ -341,7 +348,8 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
     mbar_init(&bar_full[1], kGather / 32);
     mbar_init(&bar_free[0], 1);
     mbar_init(&bar_free[1], 1);
-    mbar_init(&bar_s, 1);
+    mbar_init(&bar_s[0], 1);
+    mbar_init(&bar_s[1], 1);
     mbar_init(&bar_p, kCons / 32);
     mbar_init(&bar_o, 1);
     mbar_init(&bar_mx, kCons / 32);
@@ -428,10 +436,32 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
   __syncthreads();
   tc_fence_after();
 
-  if (warp == kProdWarp) {
-    // ================= producer warp: MMA issue =============================
-    const uint64_t dq0 = smem_desc(sQ, 16, 1024, kSw128);
-    const uint64_t dp0 = smem_desc(sP, 16, 1024, kSw128);
+  const uint64_t dq0 = smem_desc(sQ, 16, 1024, kSw128);
+  const uint64_t dp0 = smem_desc(sP, 16, 1024, kSw128);
+  // S = Q . K^T of local tile tt for its tokens 32 h2 .. 32 h2 + 31 (one
+  // thread): 36 k-steps of N = 32.  Two threads in two warps issue the two
+  // halves side by side; their rows start 32 rows (4 KiB, whole swizzle
+  // atoms) into every column block of the stage.
+  auto issue_s = [&](int tt, int h2) {
+    const uint64_t dk0 = smem_desc(sK + (uint32_t)(tt & 1) * kKStageBytes + (uint32_t)h2 * 32 * 128,
+                                   16, 1024, kSw128);
+    const uint32_t d = tmem + kTmemS + (uint32_t)h2 * (kTile / 2);
+#pragma unroll
+    for (int kk = 0; kk < kDK / 16; ++kk) {
+      const uint64_t db = dk0 + (uint64_t)(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4);
+      if (kk < kQTmemDims / 16) {
+        mma_bf16_ta(d, tmem + kTmemQ + kk * 8, db, kIdescS, kk > 0 ? 1u : 0u);
+      } else {
+        const int qk = kk - kQTmemDims / 16;
+        mma_bf16(d, dq0 + (uint64_t)(((qk >> 2) * kQBlockBytes + (qk & 3) * 32) >> 4), db,
+                 kIdescS, 1u);
+      }
+    }
+    mma_commit(&bar_s[h2]);
+  };
+
+  if (warp == kProdWarp || warp == kIssueWarp) {
+    // ================= MMA issue: producer warp and second S issuer ========
     auto issue_pv = [&](int tt) {  // O += P . V(tile tt)
       const uint32_t vst = sK + (uint32_t)(tt & 1) * kKStageBytes +
                            (uint32_t)half * (kHalf / 64) * kKBlockBytes;
@@ -443,54 +473,39 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       mma_commit(&bar_o);
       mma_commit(&bar_free[tt & 1]);
     };
-    // S = Q . K^T of local tile tt into the S accumulator (one thread)
-    auto issue_s = [&](int tt) {
-      const uint64_t dk0 = smem_desc(sK + (uint32_t)(tt & 1) * kKStageBytes, 16, 1024, kSw128);
-#pragma unroll
-      for (int kk = 0; kk < kDK / 16; ++kk) {
-        const uint64_t db = dk0 + (uint64_t)(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4);
-        if (kk < kQTmemDims / 16) {
-          mma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + kk * 8, db, kIdescS, kk > 0 ? 1u : 0u);
-        } else {
-          const int qk = kk - kQTmemDims / 16;
-          mma_bf16(tmem + kTmemS,
-                   dq0 + (uint64_t)(((qk >> 2) * kQBlockBytes + (qk & 3) * 32) >> 4), db,
-                   kIdescS, 1u);
-        }
-      }
-      mma_commit(&bar_s);
-    };
     // lane 0 waits, the warp follows: control flow stays warp-uniform
     auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
       bool w = lane == 0 ? mbar_wait(bar, parity, &s_abort, budget) : true;
       __syncwarp();
       return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
     };
+    const bool prod = warp == kProdWarp;  // the producer also issues every O update
+    const int h2 = prod ? 0 : 1;
     bool ok = true;
     int last_s = -1, last_pv = -1;  // the last tiles whose S / O update was issued
     for (int t = 0; t < ntiles && ok; ++t) {
-      // 1. the previous tile's O update, as soon as its P is written (its
-      //    completion frees P, the S accumulator's reader and, on bar_free,
-      //    the previous tile's stage for the gather warps)
+      // 1. the previous tile's P is written: its O update (producer), and the
+      //    S accumulator may be rewritten (both issuers).  The O update's
+      //    completion frees P and, on bar_free, the previous tile's stage.
       if (t > 0) {
         if (!wait0(&bar_p, (t - 1) & 1)) { ok = false; break; }
-        if (lane == 0) {
+        if (prod && lane == 0) {
           tc_fence_after();
           issue_pv(t - 1);
           last_pv = t - 1;
         }
         __syncwarp();
       }
-      // 2. S = Q . K^T of this tile once the gather warps' copies landed
+      // 2. this thread's half of S = Q . K^T once the tile's gathers landed
       if (!wait0(&bar_full[t & 1], (t >> 1) & 1)) { ok = false; break; }
       if (lane == 0) {
         tc_fence_after();
-        issue_s(t);
+        issue_s(t, h2);
         last_s = t;
       }
       __syncwarp();
     }
-    if (ok) {
+    if (ok && prod) {
       if (!wait0(&bar_p, (ntiles - 1) & 1)) ok = false;
       else if (lane == 0) {
         tc_fence_after();
@@ -502,10 +517,10 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
       flag_error(err, kErrTimeout);
       s_abort = 1;
     }
-    // every MMA issued above completes before the tensor memory is freed,
-    // also when another warp gave up (normally these have completed already)
+    // every MMA this thread issued completes before the tensor memory is
+    // freed, also when another warp gave up (normally these have completed)
     if (lane == 0) {
-      if (last_s >= 0) mbar_drain(&bar_s, last_s & 1);
+      if (last_s >= 0) mbar_drain(&bar_s[h2], last_s & 1);
       if (last_pv >= 0) mbar_drain(&bar_o, last_pv & 1);
     }
     __syncwarp();
@@ -531,7 +546,7 @@ k_mla_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restrict_
         }
         tc_fence_after();
       }
-      if (!waitw(&bar_s, t & 1)) {
+      if (!waitw(&bar_s[ch], t & 1)) {  // this thread's 32 columns
         ok = false;
         break;
       }
