@@ -699,12 +699,12 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
       t.key = kstar;
       w.thr[b] = t;
     }
-    if (nch > 1) {
-      __threadfence();
-      if (atomicAdd(w.depart + b, 1) == nch - 1) {
-        w.tick[b] = 0;
-        w.depart[b] = 0;
-      }
+    // no fence: the departures only order the reset below after every CTA's
+    // last read of the arrival counter, which was an acquire load that this
+    // CTA's atomic cannot pass; the outputs are published by the kernel's end
+    if (nch > 1 && atomicAdd(w.depart + b, 1) == nch - 1) {
+      w.tick[b] = 0;
+      w.depart[b] = 0;
     }
   }
 }
