@@ -63,6 +63,18 @@ def test_paging_example_variants(over):
 
 
 @pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
+def test_one_and_several_chunk_requests_together(topk_mode):
+    # requests of one 4096-token top-k chunk (no request barrier in the
+    # single launch) beside requests of two and three chunks, sparse and dense
+    lens = (4096, 4097, 8192, 100, 12288, 300)
+    wl = WORKLOADS["paging_example"].replace(
+        B=len(lens), seq_lens=lens, k=300, page_size=64, num_pages=3 * 193 + 16,
+        max_pages=192)
+    t, _, _ = prepare(wl)
+    full_check(wl, t, topk_mode=topk_mode)
+
+
+@pytest.mark.parametrize("topk_mode", [0, 1], ids=["coop", "two_kernel"])
 def test_all_scores_tied(topk_mode):
     # zero indexer queries: every score is 0, selection = lowest indices
     wl = WORKLOADS["paging_example"]
