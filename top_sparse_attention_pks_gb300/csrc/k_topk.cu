@@ -247,14 +247,14 @@ __device__ __forceinline__ void request_arrive(int32_t* arrive) {
 }
 
 // Bounded wait until `count` CTAs of a request have arrived (one thread).
+// Every arrival is a fence and an atomic add (a release), so the acquire load
+// that sees the full count orders this thread's later reads after all the
+// arrivers' writes; the CTA's other threads follow it through __syncthreads.
 __device__ __forceinline__ bool request_wait(int32_t* arrive, int count, int spins) {
   for (int it = 0; it < spins; ++it) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(arrive) : "memory");
-    if (v >= count) {
-      __threadfence();
-      return true;
-    }
+    if (v >= count) return true;
     if (it >= 32) __nanosleep(64);
   }
   return false;
@@ -692,13 +692,6 @@ k_topk_select(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ 
   // the last CTA to leave resets the request's barrier counters
   __syncthreads();
   if (tid == 0) {
-    if (c == 0) {
-      TopkThreshold t;
-      t.bin = T1;
-      t.pad = 0;
-      t.key = kstar;
-      w.thr[b] = t;
-    }
     // no fence: the departures only order the reset below after every CTA's
     // last read of the arrival counter, which was an acquire load that this
     // CTA's atomic cannot pass; the outputs are published by the kernel's end
