@@ -218,9 +218,15 @@ k_sparse_attention(const int32_t* __restrict__ seq_lens, const int32_t* __restri
   if (cta == 0) {
     for (int i = tid; i <= B; i += NT) prefix_out[i] = s_prefix[i];
     if (tid == 0) prefix_out[B + 1] = (int32_t)GRID;
-    for (int b = 0; b < B; ++b) {
-      if (s_prefix[b + 1] != s_prefix[b]) continue;
-      for (int i = tid; i < Hq * D; i += NT) out[(int64_t)b * Hq * D + i] = __float2bfloat16(0.f);
+    // a thread a request finds the empty ones; the CTA zeroes them together
+    // (normally there are none, and the check costs one barrier per NT requests)
+    for (int b0 = 0; b0 < B; b0 += NT) {
+      const int b = b0 + tid;
+      if (!__syncthreads_or(b < B && s_prefix[b + 1] == s_prefix[b])) continue;
+      for (int bb = b0; bb < B && bb < b0 + NT; ++bb) {
+        if (s_prefix[bb + 1] != s_prefix[bb]) continue;
+        for (int i = tid; i < Hq * D; i += NT) out[(int64_t)bb * Hq * D + i] = __float2bfloat16(0.f);
+      }
     }
   }
   if (T == 0 || cta >= GRID) return;
