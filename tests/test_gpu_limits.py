@@ -36,10 +36,20 @@ def test_largest_batch():
     wl = WORKLOADS["paging_example"].replace(B=4096, seq_lens=lens, k=48, page_size=16,
                                              max_pages=13, num_pages=4096 * 13)
     t, _, _ = prepare(wl)
-    step, out, ref_idx = _check(wl, t)
+    step = SparseDecodeStep(t, wl.k)
+    step.out.fill_(float("nan"))  # every output must be written, empty requests too
+    out, idx = step()
+    torch.cuda.synchronize()
+    assert step.device_error() == 0
+    _, ref_idx = oracle_topk(wl, t)
+    assert (host(idx).numpy() == ref_idx).all(), "top-k"
     req = list(range(0, 4096, 97)) + [4095]
     o = out[torch.as_tensor(req, device=out.device)]
     check_attention(o, oracle_attention(wl, t, ref_idx, requests=req), "B = 4096")
+    # requests of length 0 (spread over the whole batch) get zero outputs
+    empty = [b for b, n in enumerate(lens) if n == 0]
+    assert any(b >= 256 for b in empty)
+    assert (out[torch.as_tensor(empty, device=out.device)].float() == 0).all()
 
 
 def test_largest_k():
